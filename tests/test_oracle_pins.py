@@ -1,0 +1,386 @@
+"""Pins for the fp64 oracle, against what the pages and the mathematics fix.
+
+Each test is chosen so that a plausible mistake in the oracle (a dropped term,
+a wrong index, a wrong sign, a transposed operand, a wrong softmax base or
+scale) fails at least one of them.  None of them compares the oracle with a
+retyped copy of its own formula.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+UNITS = {"B": 1, "KiB": 2**10, "MiB": 2**20, "GiB": 2**30, "MB": 1e6, "GB": 1e9}
+
+
+def _f64_cache(rng, shape):
+    return rng.standard_normal(shape)
+
+
+def _paged(x_seq, block_size, table):
+    """Scatter a contiguous [S, ...] sequence into blocks named by table (test helper)."""
+    S = x_seq.shape[0]
+    nb = int(max(table)) + 1
+    out = np.full((nb, block_size) + x_seq.shape[1:], np.nan)
+    for t in range(S):
+        out[table[t // block_size], t % block_size] = x_seq[t]
+    return out
+
+
+# ---------------------------------------------------------------- element decoding
+
+def test_half_decoding_matches_numpy_for_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = oracle.half_to_double(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_bf16_decoding_matches_torch_for_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.bf16_to_double(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# ---------------------------------------------------------------- cache-size formulas
+
+def _golden_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "cache_sizes.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            body, cite = line.split("|", 1)
+            tok = body.split()
+            rows.append((tok[0], tok[1], [int(x) for x in tok[2:8]], float(tok[8]), tok[9],
+                         float(tok[10]), cite.strip()))
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_rows(), ids=lambda r: r[0])
+def test_cache_size_formulas_match_printed_values(row):
+    name, kind, (n_layers, a, b, nbytes, tokens, batch), printed, unit, tol, cite = row
+    if kind == "kv":
+        per_token = oracle.kv_bytes_per_token(n_layers, a, b, nbytes)
+    else:
+        per_token = oracle.mla_bytes_per_token(n_layers, a, b, nbytes)
+    total = per_token * tokens * batch
+    value = total / UNITS[unit]
+    if tol == 0:
+        assert value == printed, (name, value, printed, cite)
+    else:
+        assert abs(value - printed) <= tol * printed + 1e-12, (name, value, printed, cite)
+
+
+def test_mla_vs_mha_ratio_and_gqa_equivalent_heads():
+    # 576 vs 32768 elements per token per layer: "roughly a 57x difference",
+    # "approximately 2.25 GQA KV heads" (576 / (2 x 128)).
+    mla = oracle.mla_bytes_per_token(1, 512, 64, 1)
+    mha = oracle.kv_bytes_per_token(1, 128, 128, 1)
+    assert round(mha / mla) == 57
+    assert mla / oracle.kv_bytes_per_token(1, 1, 128, 1) == 2.25
+
+
+def test_convexity_of_the_kv_head_dial():
+    # 32 -> 8 KV heads removes 75% of the cache, 8 -> 1 removes about 22 points more.
+    full = oracle.kv_bytes_per_token(32, 32, 128, 2)
+    g8 = oracle.kv_bytes_per_token(32, 8, 128, 2)
+    g1 = oracle.kv_bytes_per_token(32, 1, 128, 2)
+    assert (full - g8) / full == 0.75
+    assert round(100 * (g8 - g1) / full) == 22
+
+
+# ---------------------------------------------------------------- GQA decode pins
+
+def _gqa(q, k, v, bt, sl, scale, **kw):
+    return oracle.gqa_decode(q, k, v, bt, sl, dtype="f64", scale=scale, **kw)
+
+
+def test_paged_gather_equals_contiguous_sequence():
+    """Scattering a contiguous sequence into permuted blocks must not change anything."""
+    rng = np.random.default_rng(1)
+    S, bs, h_kv, d, h_q = 37, 4, 2, 8, 4
+    kseq = rng.standard_normal((S, h_kv, d))
+    vseq = rng.standard_normal((S, h_kv, d))
+    q = rng.standard_normal((1, h_q, d))
+    nblk = math.ceil(S / bs)
+    # contiguous: identity table over a [nblk, bs] layout
+    ident = np.arange(nblk, dtype=np.int32)
+    kc = _paged(kseq, bs, ident)
+    vc = _paged(vseq, bs, ident)
+    kc[np.isnan(kc)] = 0.0
+    vc[np.isnan(vc)] = 0.0
+    o1, l1 = _gqa(q, kc, vc, ident[None], np.array([S], np.int32), 0.3)
+    # permuted blocks, with spare never-referenced blocks full of NaN
+    perm = rng.permutation(nblk + 5)[:nblk].astype(np.int32)
+    kp = _paged(kseq, bs, perm)
+    vp = _paged(vseq, bs, perm)
+    o2, l2 = _gqa(q, kp, vp, perm[None], np.array([S], np.int32), 0.3)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_cache_row_inverse_of_scatter():
+    table = np.array([[5, 2, 7]], dtype=np.int32)
+    # token 9 with block_size 4 sits in logical block 2 -> physical 7, slot 1
+    assert oracle.cache_row(table, 4, 8, 0, 9) == 7 * 4 + 1
+    assert oracle.cache_row(table, 4, 8, 0, 0) == 5 * 4
+    assert oracle.cache_row(np.array([[9]], np.int32), 4, 8, 0, 0) == -1
+
+
+@pytest.mark.parametrize("h_q,h_kv", [(8, 2), (8, 1), (8, 8), (12, 3)])
+def test_gqa_equals_mha_on_repeat_interleaved_kv(h_q, h_kv):
+    """Indexing KV head i // (h_q/h_kv) equals MHA on K/V with each head repeated."""
+    rng = np.random.default_rng(2)
+    S, bs, d = 19, 4, 16
+    nb = math.ceil(S / bs)
+    k = rng.standard_normal((nb, bs, h_kv, d))
+    v = rng.standard_normal((nb, bs, h_kv, d))
+    q = rng.standard_normal((2, h_q, d))
+    bt = np.stack([np.arange(nb), np.arange(nb)[::-1]]).astype(np.int32)
+    sl = np.array([S, S - 6], np.int32)
+    o_g, l_g = _gqa(q, k, v, bt, sl, 0.25)
+    rep = h_q // h_kv
+    k_rep = np.repeat(k, rep, axis=2)  # repeat_interleave along the head axis
+    v_rep = np.repeat(v, rep, axis=2)
+    o_m, l_m = _gqa(q, k_rep, v_rep, bt, sl, 0.25)
+    assert np.array_equal(o_g, o_m) and np.array_equal(l_g, l_m)
+    if 1 < h_kv < h_q:
+        # sensitivity: the interleaved-modulo mapping (head i -> i % h_kv) is different
+        o_bad, _ = _gqa(q, np.tile(k, (1, 1, rep, 1)), np.tile(v, (1, 1, rep, 1)), bt, sl, 0.25)
+        assert not np.allclose(o_bad, o_g)
+
+
+def test_single_token_returns_its_value_exactly():
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal((2, 4, 2, 8))
+    v = rng.standard_normal((2, 4, 2, 8))
+    q = rng.standard_normal((1, 4, 8))
+    bt = np.array([[1, 0]], np.int32)
+    out, lse = _gqa(q, k, v, bt, np.array([1], np.int32), 0.5)
+    for i in range(4):
+        j = i // 2
+        assert np.array_equal(out[i], v[1, 0, j])
+        assert lse[i] == pytest.approx(0.5 * float(q[0, i] @ k[1, 0, j]), abs=1e-14)
+
+
+def test_zero_query_gives_mean_of_values_and_log_length():
+    rng = np.random.default_rng(4)
+    S, bs = 23, 8
+    k = rng.standard_normal((3, bs, 1, 8))
+    v = rng.standard_normal((3, bs, 1, 8))
+    q = np.zeros((1, 2, 8))
+    bt = np.array([[2, 0, 1]], np.int32)
+    out, lse = _gqa(q, k, v, bt, np.array([S], np.int32), 1.0)
+    vals = np.stack([v[bt[0, t // bs], t % bs, 0] for t in range(S)])
+    for i in range(2):
+        np.testing.assert_allclose(out[i], vals.mean(axis=0), rtol=0, atol=1e-14)
+        assert lse[i] == pytest.approx(math.log(S), abs=1e-14)
+
+
+def test_equal_keys_give_mean_and_constant_values_are_reproduced():
+    rng = np.random.default_rng(5)
+    S = 9
+    kvec = rng.standard_normal(8)
+    k = np.broadcast_to(kvec, (S, 1, 1, 8)).copy().reshape(S, 1, 1, 8)
+    v = rng.standard_normal((S, 1, 1, 8))
+    q = rng.standard_normal((1, 1, 8))
+    bt = np.arange(S, dtype=np.int32)[None]
+    out, lse = _gqa(q, k, v, bt, np.array([S], np.int32), 0.7)
+    np.testing.assert_allclose(out[0], v[:, 0, 0].mean(axis=0), atol=1e-14)
+    assert lse[0] == pytest.approx(0.7 * float(q[0, 0] @ kvec) + math.log(S), abs=1e-13)
+    # constant values: the probabilities sum to one
+    k2 = rng.standard_normal((S, 1, 1, 8))
+    vc = np.full((S, 1, 1, 8), -1.75)
+    out2, _ = _gqa(q, k2, vc, bt, np.array([S], np.int32), 0.7)
+    np.testing.assert_allclose(out2[0], -1.75, atol=1e-14)
+
+
+def test_two_tokens_closed_form():
+    # q = e0, k0 = 2 e0, k1 = 0, scale 1/2 -> s0 = 1, s1 = 0
+    # p0 = e/(1+e), p1 = 1/(1+e); v0 = e0, v1 = e1.
+    d = 4
+    q = np.zeros((1, 1, d)); q[0, 0, 0] = 1.0
+    k = np.zeros((2, 1, 1, d)); k[0, 0, 0, 0] = 2.0
+    v = np.zeros((2, 1, 1, d)); v[0, 0, 0, 0] = 1.0; v[1, 0, 0, 1] = 1.0
+    bt = np.array([[0, 1]], np.int32)
+    out, lse = _gqa(q, k, v, bt, np.array([2], np.int32), 0.5)
+    e = math.e
+    assert out[0, 0] == pytest.approx(e / (1 + e), abs=1e-15)
+    assert out[0, 1] == pytest.approx(1 / (1 + e), abs=1e-15)
+    assert out[0, 2] == 0.0 and out[0, 3] == 0.0
+    assert lse[0] == pytest.approx(math.log(1 + e), abs=1e-15)
+
+
+def test_softmax_weights_follow_exponential_of_scaled_scores():
+    # one-hot query and keys: s_t = scale * c_t; one-hot values read p back.
+    S, d = 6, 8
+    c = np.array([0.0, 3.0, -2.0, 1.5, 3.0, -7.0])
+    q = np.zeros((1, 1, d)); q[0, 0, 2] = 1.0
+    k = np.zeros((S, 1, 1, d)); k[:, 0, 0, 2] = c
+    v = np.zeros((S, 1, 1, d))
+    for t in range(S):
+        v[t, 0, 0, t] = 1.0
+    scale = 0.8
+    bt = np.arange(S, dtype=np.int32)[None]
+    out, lse = _gqa(q, k, v, bt, np.array([S], np.int32), scale)
+    z = math.fsum(math.exp(scale * x) for x in c)
+    for t in range(S):
+        assert out[0, t] == pytest.approx(math.exp(scale * c[t]) / z, rel=1e-14)
+    assert lse[0] == pytest.approx(math.log(z), abs=1e-14)
+
+
+def test_large_scores_select_the_argmax_value():
+    rng = np.random.default_rng(6)
+    S, d = 12, 16
+    k = rng.standard_normal((S, 1, 1, d)) * 0.01
+    k[7, 0, 0] = 0.0
+    k[7, 0, 0, 3] = 1.0
+    q = np.zeros((1, 1, d)); q[0, 0, 3] = 1.0
+    v = rng.standard_normal((S, 1, 1, d))
+    bt = np.arange(S, dtype=np.int32)[None]
+    out, _ = _gqa(q, k, v, bt, np.array([S], np.int32), 60.0)
+    np.testing.assert_allclose(out[0], v[7, 0, 0], atol=1e-20 + 1e-12)
+
+
+@pytest.mark.parametrize("split", [0, 1, 5, 16, 31, 32])
+def test_lse_merge_of_halves_equals_whole(split):
+    rng = np.random.default_rng(7)
+    S, bs, d, h_q = 32, 4, 8, 4
+    k = rng.standard_normal((8, bs, 2, d)) * 2
+    v = rng.standard_normal((8, bs, 2, d))
+    q = rng.standard_normal((1, h_q, d))
+    bt = rng.permutation(8).astype(np.int32)[None]
+    sl = np.array([S], np.int32)
+    whole, lw = _gqa(q, k, v, bt, sl, 0.9)
+    a, la = _gqa(q, k, v, bt, sl, 0.9, t_begin=0, t_end=split)
+    b, lb = _gqa(q, k, v, bt, sl, 0.9, t_begin=split, t_end=-1)
+    for i in range(h_q):
+        m, lm = oracle.lse_merge(np.stack([a[i], b[i]]), np.array([la[i], lb[i]]))
+        np.testing.assert_allclose(m, whole[i], atol=1e-13)
+        assert lm == pytest.approx(lw[i], abs=1e-13)
+
+
+def test_token_order_does_not_matter():
+    rng = np.random.default_rng(8)
+    S, d = 15, 8
+    kseq = rng.standard_normal((S, 1, 1, d))
+    vseq = rng.standard_normal((S, 1, 1, d))
+    q = rng.standard_normal((1, 2, d))
+    perm = rng.permutation(S)
+    bt = np.arange(S, dtype=np.int32)[None]
+    o1, l1 = _gqa(q, kseq, vseq, bt, np.array([S], np.int32), 0.6)
+    o2, l2 = _gqa(q, kseq[perm], vseq[perm], bt, np.array([S], np.int32), 0.6)
+    np.testing.assert_allclose(o1, o2, atol=1e-14)
+    np.testing.assert_allclose(l1, l2, atol=1e-14)
+
+
+def test_empty_sequence_and_bad_block():
+    k = np.ones((2, 4, 1, 8))
+    q = np.ones((2, 1, 8))
+    bt = np.array([[0, 1], [1, 5]], np.int32)
+    out, lse = _gqa(q, k, k, bt, np.array([0, 4], np.int32), 1.0)
+    assert np.all(out[0] == 0.0) and lse[0] == -math.inf
+    with pytest.raises(ValueError):
+        _gqa(q, k, k, bt, np.array([0, 6], np.int32), 1.0)  # token 4 reads block id 5 >= 2
+
+
+def test_oracle_reads_16bit_storage_like_its_decoded_values():
+    rng = np.random.default_rng(9)
+    kf = rng.standard_normal((3, 4, 2, 8)).astype(np.float16)
+    vf = rng.standard_normal((3, 4, 2, 8)).astype(np.float16)
+    qf = rng.standard_normal((1, 4, 8)).astype(np.float16)
+    bt = np.array([[2, 0, 1]], np.int32)
+    sl = np.array([11], np.int32)
+    o16, l16 = oracle.gqa_decode(qf.view(np.uint16), kf.view(np.uint16), vf.view(np.uint16), bt,
+                                 sl, dtype="fp16", scale=0.4)
+    o64, l64 = _gqa(qf.astype(np.float64), kf.astype(np.float64), vf.astype(np.float64), bt, sl,
+                    0.4)
+    assert np.array_equal(o16, o64) and np.array_equal(l16, l64)
+
+
+# ---------------------------------------------------------------- MLA pins
+
+def test_absorbed_mla_matches_explicit_reconstruction():
+    """Reconstruct-then-attend equals the absorbed form (the pages' MLA exercise)."""
+    rng = np.random.default_rng(10)
+    h, d_c, d_h, d_r, d_v, S = 4, 32, 16, 8, 16, 7
+    q_nope = rng.standard_normal((h, d_h))
+    q_rope = rng.standard_normal((h, d_r))
+    c = rng.standard_normal((S, d_c))
+    kr = rng.standard_normal((S, d_r))
+    w_uk = rng.standard_normal((h, d_c, d_h)) / math.sqrt(d_c)
+    w_uv = rng.standard_normal((h, d_c, d_v)) / math.sqrt(d_c)
+    scale = 1.0 / math.sqrt(d_h + d_r)
+    out_x, scores_x = oracle.mla_explicit(q_nope, q_rope, c, kr, w_uk, w_uv, scale=scale)
+    # absorbed: q_abs^(i) = W_uk^(i) q_nope^(i) (a d_c vector); cache = [c | kr]
+    q_abs = np.einsum("iae,ie->ia", w_uk, q_nope)[None]
+    cache = np.concatenate([c, kr], axis=1)[:, None, :]  # block_size 1
+    bt = np.arange(S, dtype=np.int32)[None]
+    lat, lse = oracle.mla_decode(q_abs, q_rope[None], cache, bt, np.array([S], np.int32),
+                                 dtype="f64", scale=scale)
+    out_a = np.einsum("ia,iav->iv", lat, w_uv)
+    np.testing.assert_allclose(out_a, out_x, rtol=1e-10, atol=1e-12)
+    m = scores_x.max(axis=1)
+    lse_x = m + np.log(np.exp(scores_x - m[:, None]).sum(axis=1))
+    np.testing.assert_allclose(lse, lse_x, rtol=1e-10)
+
+
+def test_mla_without_rope_is_mqa_with_latent_as_key_and_value():
+    rng = np.random.default_rng(11)
+    H, d_c, S, bs = 6, 16, 21, 4
+    nb = math.ceil(S / bs) + 2
+    lat = rng.standard_normal((nb, bs, d_c))
+    cache = np.concatenate([lat, rng.standard_normal((nb, bs, 4))], axis=2)
+    q_abs = rng.standard_normal((1, H, d_c))
+    q_rope = np.zeros((1, H, 4))
+    bt = rng.permutation(nb)[: math.ceil(S / bs)].astype(np.int32)[None]
+    sl = np.array([S], np.int32)
+    o_mla, l_mla = oracle.mla_decode(q_abs, q_rope, cache, bt, sl, dtype="f64", scale=0.3)
+    o_mqa, l_mqa = _gqa(q_abs, lat[:, :, None, :], lat[:, :, None, :], bt, sl, 0.3)
+    np.testing.assert_allclose(o_mla, o_mqa, atol=1e-14)
+    np.testing.assert_allclose(l_mla, l_mqa, atol=1e-14)
+
+
+def test_mla_rope_part_closed_form():
+    # q_abs = 0; q_rope = a e0; kr_0 = e0, kr_1 = 0 -> s0 = scale a, s1 = 0
+    d_c, d_r = 8, 4
+    a, scale = 3.0, 0.5
+    q_abs = np.zeros((1, 1, d_c))
+    q_rope = np.zeros((1, 1, d_r)); q_rope[0, 0, 0] = a
+    cache = np.zeros((2, 1, d_c + d_r))
+    cache[0, 0, :d_c] = np.arange(1, d_c + 1)
+    cache[1, 0, :d_c] = -1.0
+    cache[0, 0, d_c] = 1.0
+    bt = np.array([[0, 1]], np.int32)
+    out, lse = oracle.mla_decode(q_abs, q_rope, cache, bt, np.array([2], np.int32), dtype="f64",
+                                 scale=scale)
+    p0 = 1.0 / (1.0 + math.exp(-scale * a))
+    np.testing.assert_allclose(out[0], p0 * np.arange(1, d_c + 1) + (1 - p0) * -1.0, atol=1e-14)
+    assert lse[0] == pytest.approx(math.log(math.exp(scale * a) + 1.0), abs=1e-14)
+
+
+def test_mla_latent_part_closed_form():
+    # q_abs = e3; latent of token 0 = 2 e3 + 5 e0, of token 1 = 0; rope ignored (q_rope = 0)
+    d_c, d_r = 8, 4
+    q_abs = np.zeros((1, 1, d_c)); q_abs[0, 0, 3] = 1.0
+    q_rope = np.zeros((1, 1, d_r))
+    cache = np.zeros((2, 2, d_c + d_r))
+    cache[1, 0, 3] = 2.0; cache[1, 0, 0] = 5.0
+    cache[1, 0, d_c:] = 100.0  # rope key: multiplied by a zero query
+    bt = np.array([[1]], np.int32)
+    out, _ = oracle.mla_decode(q_abs, q_rope, cache, bt, np.array([2], np.int32), dtype="f64",
+                               scale=1.0)
+    p0 = math.exp(2.0) / (math.exp(2.0) + 1.0)
+    expect = np.zeros(d_c); expect[3] = 2.0 * p0; expect[0] = 5.0 * p0
+    np.testing.assert_allclose(out[0], expect, atol=1e-14)
