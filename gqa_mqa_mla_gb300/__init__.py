@@ -1,0 +1,25 @@
+"""libdecattn: GB300-native single-token decode attention over a paged KV cache.
+
+MHA / GQA / MQA (``gqa_decode``) and absorbed MLA (``mla_decode``), hand-written
+CUDA kernels for sm_103a behind a C ABI (include/decattn.h).  This package is
+the thin Python binding; ``synth`` draws seeded synthetic inputs.
+"""
+from .binding import (  # noqa: F401
+    DecAttnError,
+    FLAG_BAD_BLOCK,
+    FLAG_BAD_SEQ_LEN,
+    FLAG_TIMEOUT,
+    gqa_decode,
+    gqa_plan_splits,
+    gqa_workspace_size,
+    kv_bytes_per_token,
+    lib,
+    library_path,
+    mla_bytes_per_token,
+    mla_decode,
+    mla_plan_splits,
+    mla_workspace_size,
+    status_string,
+)
+
+__version__ = "0.1.0"

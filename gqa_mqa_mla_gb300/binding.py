@@ -1,0 +1,234 @@
+"""ctypes binding of libdecattn (include/decattn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and the current
+stream.  If the shared library is missing the calls raise; there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+DECATTN_OK = 0
+DECATTN_ERR_INVALID_ARG = -1
+DECATTN_ERR_UNSUPPORTED = -2
+DECATTN_ERR_WORKSPACE = -3
+DECATTN_ERR_CUDA = -4
+DECATTN_FP16 = 0
+DECATTN_BF16 = 1
+FLAG_BAD_BLOCK = 1
+FLAG_BAD_SEQ_LEN = 2
+FLAG_TIMEOUT = 4
+MAX_SPLITS = 256
+
+MLA_HEADS, MLA_D_C, MLA_D_R = 128, 512, 64
+
+_DT = {torch.float16: DECATTN_FP16, torch.bfloat16: DECATTN_BF16}
+
+
+class DecAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+class Launch(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int),
+        ("num_blocks", ctypes.c_int),
+        ("block_size", ctypes.c_int),
+        ("max_blocks_per_seq", ctypes.c_int),
+        ("max_seq_len", ctypes.c_int),
+        ("num_splits", ctypes.c_int),
+        ("dtype", ctypes.c_int),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("err_flag", ctypes.c_void_p),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libdecattn.so (built by gqa_mqa_mla_gb300.build.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with "
+                                   "`python -m gqa_mqa_mla_gb300.build` (no fallback exists)")
+            L = ctypes.CDLL(path)
+            P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            S, I64 = ctypes.c_size_t, ctypes.c_int64
+            LP = ctypes.POINTER(Launch)
+            L.gqa_decode.argtypes = [P, P, P, P, P, P, I, I, I, F, LP]
+            L.gqa_decode.restype = I
+            L.mla_decode.argtypes = [P, P, P, P, P, P, F, LP]
+            L.mla_decode.restype = I
+            L.gqa_decode_plan_splits.argtypes = [I, I, I, I, I, I]
+            L.gqa_decode_plan_splits.restype = I
+            L.mla_decode_plan_splits.argtypes = [I, I, I]
+            L.mla_decode_plan_splits.restype = I
+            L.gqa_decode_workspace_size.argtypes = [I, I, I, I]
+            L.gqa_decode_workspace_size.restype = S
+            L.mla_decode_workspace_size.argtypes = [I, I]
+            L.mla_decode_workspace_size.restype = S
+            L.decattn_kv_bytes_per_token.argtypes = [I, I, I, I]
+            L.decattn_kv_bytes_per_token.restype = I64
+            L.decattn_mla_bytes_per_token.argtypes = [I, I, I, I]
+            L.decattn_mla_bytes_per_token.restype = I64
+            L.decattn_status_string.argtypes = [I]
+            L.decattn_status_string.restype = ctypes.c_char_p
+            L.decattn_version.argtypes = []
+            L.decattn_version.restype = I
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().decattn_status_string(int(status)).decode()
+
+
+def kv_bytes_per_token(n_layers: int, n_kv: int, d_head: int, bytes_per_elem: int) -> int:
+    return int(lib().decattn_kv_bytes_per_token(n_layers, n_kv, d_head, bytes_per_elem))
+
+
+def mla_bytes_per_token(n_layers: int, d_c: int, d_rope: int, bytes_per_elem: int) -> int:
+    return int(lib().decattn_mla_bytes_per_token(n_layers, d_c, d_rope, bytes_per_elem))
+
+
+def gqa_plan_splits(batch: int, h_q: int, h_kv: int, max_seq_len: int, d_head: int = 128,
+                    num_sms: int = 0) -> int:
+    r = lib().gqa_decode_plan_splits(batch, h_q, h_kv, d_head, max_seq_len, num_sms)
+    if r < 0:
+        raise DecAttnError("gqa_decode_plan_splits", r)
+    return r
+
+
+def mla_plan_splits(batch: int, max_seq_len: int, num_sms: int = 0) -> int:
+    r = lib().mla_decode_plan_splits(batch, max_seq_len, num_sms)
+    if r < 0:
+        raise DecAttnError("mla_decode_plan_splits", r)
+    return r
+
+
+def gqa_workspace_size(batch: int, h_q: int, num_splits: int, d_head: int = 128) -> int:
+    return int(lib().gqa_decode_workspace_size(batch, h_q, d_head, num_splits))
+
+
+def mla_workspace_size(batch: int, num_splits: int) -> int:
+    return int(lib().mla_decode_workspace_size(batch, num_splits))
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_launch(batch, num_blocks, block_size, max_blocks_per_seq, max_seq_len, num_splits,
+                dtype, workspace=None, workspace_bytes=0, err_flag=None, stream=None) -> Launch:
+    return Launch(batch, num_blocks, block_size, max_blocks_per_seq, max_seq_len, num_splits,
+                  dtype, workspace, workspace_bytes, err_flag, stream)
+
+
+def gqa_decode(q, k_cache, v_cache, block_table, seq_lens, *, scale: float, max_seq_len: int,
+               out=None, num_splits: int = 0, workspace=None, err_flag=None, stream=None):
+    """MHA/GQA/MQA decode through the C ABI; returns out [B, h_q, d].
+
+    q [B, h_q, d]; k_cache/v_cache [num_blocks, block_size, h_kv, d];
+    block_table int32 [B, max_blocks]; seq_lens int32 [B]; max_seq_len a host
+    upper bound of seq_lens.  workspace: optional uint8 CUDA tensor (sized by
+    gqa_workspace_size); allocated here when needed and not given.
+    """
+    _check(q, "q", ndim=3)
+    _check(k_cache, "k_cache", q.dtype, 4)
+    _check(v_cache, "v_cache", q.dtype, 4)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    if q.dtype not in _DT:
+        raise TypeError("q must be float16 or bfloat16")
+    B, h_q, d = q.shape
+    nb, bs, h_kv, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache / v_cache shape mismatch")
+    if h_kv < 1 or h_q % h_kv != 0:
+        raise ValueError(f"h_q={h_q} is not a multiple of h_kv={h_kv}")
+    if out is None:
+        out = torch.empty_like(q)
+    ns = num_splits if num_splits else gqa_plan_splits(B, h_q, h_kv, max_seq_len, d)
+    need = gqa_workspace_size(B, h_q, ns, d)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    L = make_launch(B, nb, bs, block_table.shape[1], max_seq_len, ns, _DT[q.dtype],
+                    _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                    _ptr(err_flag), _stream_handle(stream))
+    st = lib().gqa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                          block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(), h_q, h_kv,
+                          d, float(scale), ctypes.byref(L))
+    if st != DECATTN_OK:
+        raise DecAttnError("gqa_decode", st)
+    return out
+
+
+def mla_decode(q_absorbed, q_rope, latent_cache, block_table, seq_lens, *, scale: float,
+               max_seq_len: int, out=None, num_splits: int = 0, workspace=None, err_flag=None,
+               stream=None):
+    """Absorbed MLA decode through the C ABI; returns out [B, 128, 512]."""
+    _check(q_absorbed, "q_absorbed", ndim=3)
+    _check(q_rope, "q_rope", q_absorbed.dtype, 3)
+    _check(latent_cache, "latent_cache", q_absorbed.dtype, 3)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    if q_absorbed.dtype not in _DT:
+        raise TypeError("q_absorbed must be float16 or bfloat16")
+    B = q_absorbed.shape[0]
+    if q_absorbed.shape != (B, MLA_HEADS, MLA_D_C) or q_rope.shape != (B, MLA_HEADS, MLA_D_R):
+        raise ValueError("q_absorbed must be [B,128,512] and q_rope [B,128,64]")
+    nb, bs, width = latent_cache.shape
+    if width != MLA_D_C + MLA_D_R:
+        raise ValueError("latent_cache must be [num_blocks, block_size, 576]")
+    if out is None:
+        out = torch.empty_like(q_absorbed)
+    ns = num_splits if num_splits else mla_plan_splits(B, max_seq_len)
+    need = mla_workspace_size(B, ns)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_absorbed.device)
+    L = make_launch(B, nb, bs, block_table.shape[1], max_seq_len, ns, _DT[q_absorbed.dtype],
+                    _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                    _ptr(err_flag), _stream_handle(stream))
+    st = lib().mla_decode(q_absorbed.data_ptr(), q_rope.data_ptr(), latent_cache.data_ptr(),
+                          block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
+                          float(scale), ctypes.byref(L))
+    if st != DECATTN_OK:
+        raise DecAttnError("mla_decode", st)
+    return out

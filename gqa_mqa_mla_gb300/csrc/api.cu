@@ -1,0 +1,330 @@
+// api.cu -- the C ABI of libdecattn: argument checks, split planning,
+// workspace carving, TMA descriptor construction and kernel dispatch.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "decattn.h"
+#include "internal.h"
+
+namespace decattn {
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int ilog2(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D tensor map over a row-major [outer, inner] 16-bit tensor whose rows are
+// row_bytes apart; boxes of box_inner x box_outer elements, 128-byte swizzle.
+bool make_map_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+// Token chunk per split: a multiple of kTile covering max_seq_len in at most
+// n_split chunks.  Returns the number of chunks actually used.
+int resolve_splits(int max_seq_len, int n_split, int* tokens_per_split) {
+  const int tiles = max_seq_len > 0 ? (max_seq_len + kTile - 1) / kTile : 1;
+  if (n_split < 1) n_split = 1;
+  if (n_split > tiles) n_split = tiles;
+  const int tiles_per = (tiles + n_split - 1) / n_split;
+  *tokens_per_split = tiles_per * kTile;
+  return (tiles + tiles_per - 1) / tiles_per;
+}
+
+// Choose the split count minimising an estimated makespan: waves of CTAs
+// (slots = SMs x resident CTAs) times the tiles each CTA streams plus a fixed
+// per-CTA overhead, plus the combine pass when splitting.
+int plan_splits(int units, int max_seq_len, int slots, double overhead_tiles,
+                double combine_tiles) {
+  const int tiles = max_seq_len > 0 ? (max_seq_len + kTile - 1) / kTile : 1;
+  if (slots < 1) slots = 1;
+  int best = 1;
+  double best_cost = 1e300;
+  const int cap = tiles < DECATTN_MAX_SPLITS ? tiles : DECATTN_MAX_SPLITS;
+  for (int ns = 1; ns <= cap; ++ns) {
+    int tps = 0;
+    const int eff = resolve_splits(max_seq_len, ns, &tps);
+    if (eff != ns) continue;
+    const double ctas = static_cast<double>(units) * eff;
+    const double waves = std::ceil(ctas / slots);
+    double cost = waves * (tps / kTile + overhead_tiles);
+    if (eff > 1) cost += combine_tiles;
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = eff;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+int plan_gqa_splits(int batch, int /*h_q*/, int h_kv, int max_seq_len, int num_sms) {
+  // GQA partial kernel: two resident CTAs per SM (3-stage ring of 32 KB).
+  return plan_splits(batch * h_kv, max_seq_len, num_sms * 2, 1.5, 1.0);
+}
+
+int plan_mla_splits(int batch, int max_seq_len, int num_sms) {
+  // MLA partial kernel: one CTA pair per two SMs.
+  return plan_splits(batch, max_seq_len, num_sms / 2, 2.0, 1.0);
+}
+
+}  // namespace decattn
+
+using namespace decattn;
+
+extern "C" {
+
+const char* decattn_status_string(int status) {
+  switch (status) {
+    case DECATTN_OK: return "ok";
+    case DECATTN_ERR_INVALID_ARG: return "invalid argument";
+    case DECATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DECATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case DECATTN_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int decattn_version(void) { return 100; }
+
+int64_t decattn_kv_bytes_per_token(int n_layers, int n_kv, int d_head, int bytes) {
+  if (n_layers < 0 || n_kv < 0 || d_head < 0 || bytes < 0) return -1;
+  return static_cast<int64_t>(n_layers) * n_kv * d_head * 2 * bytes;
+}
+
+int64_t decattn_mla_bytes_per_token(int n_layers, int d_c, int d_rope, int bytes) {
+  if (n_layers < 0 || d_c < 0 || d_rope < 0 || bytes < 0) return -1;
+  return static_cast<int64_t>(n_layers) * (d_c + d_rope) * bytes;
+}
+
+size_t gqa_decode_workspace_size(int batch, int h_q, int d_head, int num_splits) {
+  if (batch < 1 || h_q < 1 || d_head < 1 || num_splits < 1 || num_splits > DECATTN_MAX_SPLITS)
+    return 0;
+  if (num_splits == 1) return 0;
+  const size_t rows = static_cast<size_t>(batch) * h_q * num_splits;
+  return align_up(rows * d_head * sizeof(float)) + align_up(rows * sizeof(float));
+}
+
+size_t mla_decode_workspace_size(int batch, int num_splits) {
+  return gqa_decode_workspace_size(batch, kMlaHeads, kMlaDc, num_splits);
+}
+
+int gqa_decode_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,
+                           int num_sms) {
+  if (batch < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 || d_head < 1 || max_seq_len < 0)
+    return DECATTN_ERR_INVALID_ARG;
+  if (num_sms <= 0) num_sms = device_sm_count();
+  if (num_sms <= 0) return DECATTN_ERR_CUDA;
+  return plan_gqa_splits(batch, h_q, h_kv, max_seq_len, num_sms);
+}
+
+int mla_decode_plan_splits(int batch, int max_seq_len, int num_sms) {
+  if (batch < 1 || max_seq_len < 0) return DECATTN_ERR_INVALID_ARG;
+  if (num_sms <= 0) num_sms = device_sm_count();
+  if (num_sms <= 0) return DECATTN_ERR_CUDA;
+  return plan_mla_splits(batch, max_seq_len, num_sms);
+}
+
+static int check_launch(const decattn_launch* L, bool mla) {
+  if (!L) return DECATTN_ERR_INVALID_ARG;
+  if (L->batch < 1 || L->num_blocks < 1 || L->max_blocks_per_seq < 1 || L->max_seq_len < 0)
+    return DECATTN_ERR_INVALID_ARG;
+  if (L->dtype != DECATTN_FP16 && L->dtype != DECATTN_BF16) return DECATTN_ERR_INVALID_ARG;
+  if (L->num_splits < 0 || L->num_splits > DECATTN_MAX_SPLITS) return DECATTN_ERR_INVALID_ARG;
+  if (!is_pow2(L->block_size)) return DECATTN_ERR_INVALID_ARG;
+  if (L->block_size < 8 || L->block_size > (mla ? 64 : 256)) return DECATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(L->max_seq_len) >
+      static_cast<int64_t>(L->max_blocks_per_seq) * L->block_size)
+    return DECATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(L->num_blocks) * L->block_size > 0x7fffffffLL)
+    return DECATTN_ERR_UNSUPPORTED;
+  if (L->workspace && !aligned(L->workspace, 16)) return DECATTN_ERR_INVALID_ARG;
+  if (L->err_flag && !aligned(L->err_flag, 4)) return DECATTN_ERR_INVALID_ARG;
+  return DECATTN_OK;
+}
+
+int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_table, const int32_t* seq_lens, void* out, int h_q, int h_kv,
+               int d_head, float scale, const decattn_launch* L) {
+  int st = check_launch(L, false);
+  if (st != DECATTN_OK) return st;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
+    return DECATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return DECATTN_ERR_INVALID_ARG;
+  if (h_q < 1 || h_kv < 1 || h_q % h_kv != 0) return DECATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return DECATTN_ERR_INVALID_ARG;
+  if (d_head != kHeadDim) return DECATTN_ERR_UNSUPPORTED;
+  if (h_q / h_kv > 64) return DECATTN_ERR_UNSUPPORTED;
+
+  int n_split = L->num_splits;
+  if (n_split == 0) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return DECATTN_ERR_CUDA;
+    n_split = plan_gqa_splits(L->batch, h_q, h_kv, L->max_seq_len, sms);
+  }
+  int tps = 0;
+  const int eff = resolve_splits(L->max_seq_len, n_split, &tps);
+
+  GqaParams p{};
+  p.q = q;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.err_flag = L->err_flag;
+  p.batch = L->batch;
+  p.h_q = h_q;
+  p.h_kv = h_kv;
+  p.group = h_q / h_kv;
+  p.block_size = L->block_size;
+  p.log2_block_size = ilog2(L->block_size);
+  p.num_blocks = L->num_blocks;
+  p.max_blocks_per_seq = L->max_blocks_per_seq;
+  p.max_seq_len = L->max_seq_len;
+  p.n_split = eff;
+  p.tokens_per_split = tps;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  if (eff > 1) {
+    const size_t need = gqa_decode_workspace_size(L->batch, h_q, d_head, eff);
+    if (!L->workspace || L->workspace_bytes < need) return DECATTN_ERR_WORKSPACE;
+    const size_t rows = static_cast<size_t>(L->batch) * h_q * eff;
+    p.part_o = static_cast<float*>(L->workspace);
+    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(L->workspace) +
+                                          align_up(rows * d_head * sizeof(float)));
+  }
+
+  const bool bf16 = L->dtype == DECATTN_BF16;
+  const uint64_t rows_total = static_cast<uint64_t>(L->num_blocks) * L->block_size;
+  const uint32_t box_rows = static_cast<uint32_t>(L->block_size < kTile ? L->block_size : kTile);
+  const uint64_t row_bytes = static_cast<uint64_t>(h_kv) * kHeadDim * 2;
+  CUtensorMap tk, tv;
+  if (!make_map_2d(&tk, k_cache, bf16, static_cast<uint64_t>(h_kv) * kHeadDim, rows_total,
+                   row_bytes, 64, box_rows) ||
+      !make_map_2d(&tv, v_cache, bf16, static_cast<uint64_t>(h_kv) * kHeadDim, rows_total,
+                   row_bytes, 64, box_rows))
+    return DECATTN_ERR_CUDA;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(L->stream);
+  if (launch_gqa_partial(p, tk, tv, bf16, 0, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
+  if (eff > 1) {
+    CombineParams c{p.part_o, p.part_lse, out, L->batch * h_q, eff};
+    if (launch_combine(c, kHeadDim, bf16, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
+  }
+  return DECATTN_OK;
+}
+
+int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_cache,
+               const int32_t* block_table, const int32_t* seq_lens, void* out, float scale,
+               const decattn_launch* L) {
+  int st = check_launch(L, true);
+  if (st != DECATTN_OK) return st;
+  if (!q_absorbed || !q_rope || !latent_cache || !block_table || !seq_lens || !out)
+    return DECATTN_ERR_INVALID_ARG;
+  if (!aligned(q_absorbed, 16) || !aligned(q_rope, 16) || !aligned(latent_cache, 16) ||
+      !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return DECATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return DECATTN_ERR_INVALID_ARG;
+
+  int n_split = L->num_splits;
+  if (n_split == 0) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return DECATTN_ERR_CUDA;
+    n_split = plan_mla_splits(L->batch, L->max_seq_len, sms);
+  }
+  int tps = 0;
+  const int eff = resolve_splits(L->max_seq_len, n_split, &tps);
+
+  MlaParams p{};
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.err_flag = L->err_flag;
+  p.batch = L->batch;
+  p.block_size = L->block_size;
+  p.log2_block_size = ilog2(L->block_size);
+  p.num_blocks = L->num_blocks;
+  p.max_blocks_per_seq = L->max_blocks_per_seq;
+  p.max_seq_len = L->max_seq_len;
+  p.n_split = eff;
+  p.tokens_per_split = tps;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  if (eff > 1) {
+    const size_t need = mla_decode_workspace_size(L->batch, eff);
+    if (!L->workspace || L->workspace_bytes < need) return DECATTN_ERR_WORKSPACE;
+    const size_t rows = static_cast<size_t>(L->batch) * kMlaHeads * eff;
+    p.part_o = static_cast<float*>(L->workspace);
+    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(L->workspace) +
+                                          align_up(rows * kMlaDc * sizeof(float)));
+  }
+
+  const bool bf16 = L->dtype == DECATTN_BF16;
+  const uint64_t q_rows = static_cast<uint64_t>(L->batch) * kMlaHeads;
+  const uint64_t c_rows = static_cast<uint64_t>(L->num_blocks) * L->block_size;
+  CUtensorMap tqa, tqr, tc;
+  if (!make_map_2d(&tqa, q_absorbed, bf16, kMlaDc, q_rows, kMlaDc * 2, 64, kMlaHeads) ||
+      !make_map_2d(&tqr, q_rope, bf16, kMlaDr, q_rows, kMlaDr * 2, 64, kMlaHeads) ||
+      !make_map_2d(&tc, latent_cache, bf16, kMlaWidth, c_rows, kMlaWidth * 2, 64,
+                   static_cast<uint32_t>(L->block_size)))
+    return DECATTN_ERR_CUDA;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(L->stream);
+  cudaError_t e = launch_mla_partial(p, tqa, tqr, tc, bf16, stream);
+  if (e == cudaErrorNotSupported) return DECATTN_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return DECATTN_ERR_CUDA;
+  if (eff > 1) {
+    CombineParams c{p.part_o, p.part_lse, out, L->batch * kMlaHeads, eff};
+    if (launch_combine(c, kMlaDc, bf16, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
+  }
+  return DECATTN_OK;
+}
+
+}  // extern "C"

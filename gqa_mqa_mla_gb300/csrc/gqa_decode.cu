@@ -1,0 +1,542 @@
+// gqa_decode.cu -- split-KV partial kernels for MHA / GQA / MQA decode over a
+// paged KV cache, sm_103a.
+//
+// One CTA handles one (split, KV head j, sequence b): the query heads
+// j*G .. j*G+G-1 (G = h_q / h_kv) that read KV head j ("MQA, GQA, and MLA",
+// section 8: query head i reads KV head i / (h/g), index arithmetic, no
+// copy).  Each K/V tile is fetched ONCE from HBM by TMA into shared memory
+// and reused by the whole query-head group.
+//
+// Warp roles:
+//   warp 0        producer: walks the block table (token t of sequence b is
+//                 slot t % block_size of block block_table[b][t / block_size])
+//                 and issues 2-D TMA loads of 64-token K and V tiles into a
+//                 multi-stage ring guarded by mbarriers;
+//   warps 1..W    consumers: scores, fp32 online softmax (base 2, the scale
+//                 folded with log2 e) and the P.V accumulation, each warp on
+//                 its own slice of the tile's tokens with its own (m, l, o);
+//                 the warps' states are merged through shared memory at the
+//                 end and written as the final output (one split) or as an
+//                 fp32 partial (o, lse) for the log-sum-exp combine.
+//
+// Two consumer flavours:
+//   CcConsumer<G>    CUDA cores, G <= 4: a half-warp holds one token row
+//                    (16 lanes x 16 B), warp-shuffle dot-product reductions;
+//   MmaConsumer<MT>  tensor cores (mma.sync m16n8k16) for G >= 5: the query
+//                    group padded to 16*MT rows is the A operand, K^T / V the
+//                    B operand read with ldmatrix from the swizzled tile.
+//
+// Shared-memory tile layout (written by TMA with 128-byte swizzle): a stage
+// holds K then V; each is two 64-column halves of [64 tokens][128 B], and the
+// 16-byte chunk c of row r sits at chunk (c ^ (r % 8)) of that row.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace decattn {
+namespace {
+
+constexpr int kHalfBytes = kTile * 128;         // one 64-column half of a K or V tile
+constexpr int kKvTileBytes = 2 * kHalfBytes;    // 16 KB
+constexpr int kStageBytes = 2 * kKvTileBytes;   // K + V: 32 KB
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Byte offset of 16-byte chunk c (0..15) of token row r (0..63) in a K or V tile.
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------------ CUDA-core consumer
+
+template <int G, bool kBF16>
+struct CcConsumer {
+  static constexpr int kWarps = 4;
+  static constexpr int kRowsPerWarp = G;
+
+  float q[G][8];
+  float o[G][8];
+  float m[G], l[G];
+  int chunk, half, cw;
+
+  __device__ __forceinline__ void init(const GqaParams& p, int b, int j, int cw_, int lane) {
+    cw = cw_;
+    chunk = lane & 15;  // 16-byte chunk of the 256-byte row: d = chunk*8 .. chunk*8+7
+    half = lane >> 4;   // the two half-warps take alternate tokens
+    const uint16_t* qb = static_cast<const uint16_t*>(p.q);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const size_t row = static_cast<size_t>(b) * p.h_q + j * G + g;
+      const uint4 w = *reinterpret_cast<const uint4*>(qb + row * kHeadDim + chunk * 8);
+      const float2 a = unpack2<kBF16>(w.x), bb = unpack2<kBF16>(w.y), c = unpack2<kBF16>(w.z),
+                   d = unpack2<kBF16>(w.w);
+      q[g][0] = a.x; q[g][1] = a.y; q[g][2] = bb.x; q[g][3] = bb.y;
+      q[g][4] = c.x; q[g][5] = c.y; q[g][6] = d.x; q[g][7] = d.y;
+      m[g] = kNegInf;
+      l[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ static void load8(const uint8_t* p, float (&x)[8]) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const float2 a = unpack2<kBF16>(w.x), b = unpack2<kBF16>(w.y), c = unpack2<kBF16>(w.z),
+                 d = unpack2<kBF16>(w.w);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
+  }
+
+  // Process this warp's 16 tokens (rows cw*16 .. cw*16+15) of one stage;
+  // rows >= nval are past the sequence end and are never used.
+  __device__ __forceinline__ void tile(const uint8_t* stage, int nval, float scale_log2) {
+    const uint8_t* ks = stage;
+    const uint8_t* vs = stage + kKvTileBytes;
+    float s[8][G];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = cw * 16 + 2 * i + half;
+      float k[8];
+      load8(ks + tile_off(r, chunk), k);
+      float part[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(q[g][e], k[e], acc);
+        part[g] = acc;
+      }
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) s[i][g] = (r < nval) ? part[g] * scale_log2 : kNegInf;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float mt = s[0][g];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) mt = fmaxf(mt, s[i][g]);
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+      const float m_new = fmaxf(m[g], mt);
+      const float corr = (m_new == kNegInf) ? 1.f : ex2(m[g] - m_new);
+      m[g] = m_new;
+      l[g] *= corr;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[g][e] *= corr;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = cw * 16 + 2 * i + half;
+      if (r < nval) {
+        float v[8];
+        load8(vs + tile_off(r, chunk), v);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pr = ex2(s[i][g] - m[g]);
+          l[g] += pr;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[g][e] = fmaf(pr, v[e], o[g][e]);
+        }
+      }
+    }
+  }
+
+  // Write this warp's (m, l, o) rows to the merge area.
+  __device__ __forceinline__ void finish(float* mo, float* mm, float* ml, int lane) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      l[g] += __shfl_xor_sync(0xffffffffu, l[g], 16);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], 16);
+    }
+    if (half == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float4* dst = reinterpret_cast<float4*>(mo + (cw * kRowsPerWarp + g) * kHeadDim + chunk * 8);
+        dst[0] = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+        dst[1] = make_float4(o[g][4], o[g][5], o[g][6], o[g][7]);
+      }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        mm[cw * kRowsPerWarp + g] = m[g];
+        ml[cw * kRowsPerWarp + g] = l[g];
+      }
+    }
+  }
+
+  // Does consumer warp w hold row r, and at which slot row?
+  __device__ __forceinline__ static int slot(int w, int r) { return w * kRowsPerWarp + r; }
+  __device__ __forceinline__ static bool covers(int /*w*/, int /*r*/) { return true; }
+};
+
+// ------------------------------------------------------------------ tensor-core consumer
+
+template <int MT, bool kBF16>
+struct MmaConsumer {
+  static constexpr int kWarps = MT <= 4 ? 4 : MT;
+  static constexpr int kRowsPerWarp = 16;
+  static constexpr int kWarpsPerMtile = kWarps / MT;
+  static constexpr int kTokensPerWarp = kTile / kWarpsPerMtile;
+
+  uint32_t qa[8][4];  // A fragments of the padded query group, 8 k-steps of 16
+  float o[16][4];     // 16 n-tiles of 8 head dims, rows (lane/4, lane/4+8)
+  float m[2], l[2];
+  int mt, tok0, cw, lane;
+
+  __device__ __forceinline__ void init(const GqaParams& p, int b, int j, int cw_, int lane_) {
+    cw = cw_;
+    lane = lane_;
+    mt = cw % MT;
+    tok0 = (cw / MT) * kTokensPerWarp;
+    const int G = p.group;
+    const int r_lo = mt * 16 + (lane >> 2);
+    const int r_hi = r_lo + 8;
+    const int kc = (lane & 3) * 2;
+    const uint32_t* qb = static_cast<const uint32_t*>(p.q);
+    const size_t base = (static_cast<size_t>(b) * p.h_q + static_cast<size_t>(j) * G) * kHeadDim;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int k0 = ks * 16 + kc;
+      qa[ks][0] = r_lo < G ? qb[(base + r_lo * kHeadDim + k0) >> 1] : 0u;
+      qa[ks][1] = r_hi < G ? qb[(base + r_hi * kHeadDim + k0) >> 1] : 0u;
+      qa[ks][2] = r_lo < G ? qb[(base + r_lo * kHeadDim + k0 + 8) >> 1] : 0u;
+      qa[ks][3] = r_hi < G ? qb[(base + r_hi * kHeadDim + k0 + 8) >> 1] : 0u;
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m[0] = m[1] = kNegInf;
+    l[0] = l[1] = 0.f;
+  }
+
+  __device__ __forceinline__ void tile(uint8_t* stage, int nval, float scale_log2) {
+    const uint32_t ks_base = smem_u32(stage);
+    const uint32_t vs_base = ks_base + kKvTileBytes;
+    const int t4 = lane & 3;
+#pragma unroll
+    for (int c = 0; c < kTokensPerWarp / 16; ++c) {
+      const int r0 = tok0 + 16 * c;
+      if (r0 >= nval) break;
+      if (r0 + 16 > nval) {
+        // Rows past the sequence end may hold anything (even NaN); zero the
+        // V rows so that P = 0 there contributes exactly nothing.
+        uint8_t* vs = stage + kKvTileBytes;
+        for (int idx = lane; idx < (r0 + 16 - nval) * 16; idx += 32) {
+          const int r = nval + (idx >> 4);
+          *reinterpret_cast<uint4*>(vs + tile_off(r, idx & 15)) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      // S = Q K^T for 16 tokens: two n-tiles of 8 tokens.
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int mi = lane >> 3;
+        const int tok = r0 + ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(ks_base + tile_off(tok, 2 * ks + (mi & 1)), b0, b1, b2, b3);
+          mma_16816<kBF16>(s0, qa[ks], b0, b1);
+          mma_16816<kBF16>(s1, qa[ks], b2, b3);
+        }
+      }
+      // Scale into the log2 domain and mask tokens past the end.
+      const int ta = r0 + 2 * t4, tb = r0 + 8 + 2 * t4;
+      s0[0] = ta < nval ? s0[0] * scale_log2 : kNegInf;
+      s0[1] = ta + 1 < nval ? s0[1] * scale_log2 : kNegInf;
+      s0[2] = ta < nval ? s0[2] * scale_log2 : kNegInf;
+      s0[3] = ta + 1 < nval ? s0[3] * scale_log2 : kNegInf;
+      s1[0] = tb < nval ? s1[0] * scale_log2 : kNegInf;
+      s1[1] = tb + 1 < nval ? s1[1] * scale_log2 : kNegInf;
+      s1[2] = tb < nval ? s1[2] * scale_log2 : kNegInf;
+      s1[3] = tb + 1 < nval ? s1[3] * scale_log2 : kNegInf;
+      float mx_lo = fmaxf(fmaxf(s0[0], s0[1]), fmaxf(s1[0], s1[1]));
+      float mx_hi = fmaxf(fmaxf(s0[2], s0[3]), fmaxf(s1[2], s1[3]));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      // Every chunk holds at least one valid token, so the new maxima are finite.
+      const float mn_lo = fmaxf(m[0], mx_lo), mn_hi = fmaxf(m[1], mx_hi);
+      const float c_lo = ex2(m[0] - mn_lo), c_hi = ex2(m[1] - mn_hi);
+      m[0] = mn_lo;
+      m[1] = mn_hi;
+      l[0] *= c_lo;
+      l[1] *= c_hi;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        o[n][0] *= c_lo; o[n][1] *= c_lo; o[n][2] *= c_hi; o[n][3] *= c_hi;
+      }
+      const float p00 = ex2(s0[0] - mn_lo), p01 = ex2(s0[1] - mn_lo);
+      const float p02 = ex2(s0[2] - mn_hi), p03 = ex2(s0[3] - mn_hi);
+      const float p10 = ex2(s1[0] - mn_lo), p11 = ex2(s1[1] - mn_lo);
+      const float p12 = ex2(s1[2] - mn_hi), p13 = ex2(s1[3] - mn_hi);
+      l[0] += (p00 + p01) + (p10 + p11);
+      l[1] += (p02 + p03) + (p12 + p13);
+      const uint32_t pa[4] = {pack2<kBF16>(p00, p01), pack2<kBF16>(p02, p03),
+                              pack2<kBF16>(p10, p11), pack2<kBF16>(p12, p13)};
+      // O += P V: 16 tokens x 128 dims, V read transposed by ldmatrix.
+      {
+        const int mi = lane >> 3;
+        const int tok = r0 + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int dp = 0; dp < 8; ++dp) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_trans(vs_base + tile_off(tok, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+          mma_16816<kBF16>(o[2 * dp], pa, b0, b1);
+          mma_16816<kBF16>(o[2 * dp + 1], pa, b2, b3);
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void finish(float* mo, float* mm, float* ml, int lane_) {
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
+    const int rl = lane_ >> 2, t4 = lane_ & 3;
+    float* lo = mo + (cw * kRowsPerWarp + rl) * kHeadDim;
+    float* hi = mo + (cw * kRowsPerWarp + rl + 8) * kHeadDim;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      *reinterpret_cast<float2*>(lo + n * 8 + 2 * t4) = make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(hi + n * 8 + 2 * t4) = make_float2(o[n][2], o[n][3]);
+    }
+    if (t4 == 0) {
+      mm[cw * kRowsPerWarp + rl] = m[0];
+      ml[cw * kRowsPerWarp + rl] = l[0];
+      mm[cw * kRowsPerWarp + rl + 8] = m[1];
+      ml[cw * kRowsPerWarp + rl + 8] = l[1];
+    }
+  }
+
+  __device__ __forceinline__ static bool covers(int w, int r) { return (w % MT) == (r >> 4); }
+  __device__ __forceinline__ static int slot(int w, int r) { return w * kRowsPerWarp + (r & 15); }
+};
+
+// ------------------------------------------------------------------ the kernel
+
+template <class Consumer>
+__host__ __device__ constexpr int merge_bytes() {
+  return Consumer::kWarps * Consumer::kRowsPerWarp * (kHeadDim + 2) * 4;
+}
+
+template <class Consumer, int kStages>
+__host__ __device__ constexpr int smem_bytes() {
+  return 1024 /*alignment slack*/ + kStages * kStageBytes + 256 /*barriers*/;
+}
+
+template <class Consumer, bool kBF16, int kStages>
+__global__ void __launch_bounds__(32 * (1 + Consumer::kWarps))
+    gqa_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const GqaParams p) {
+  static_assert(merge_bytes<Consumer>() <= kStages * kStageBytes, "merge area must fit the ring");
+  constexpr int kW = Consumer::kWarps;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + kStages);
+  const uint32_t done_bar = smem_u32(bars + 2 * kStages);
+  const uint32_t merge_bar = smem_u32(bars + 2 * kStages + 1);
+
+  const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.group;
+
+  const int seq_len = p.seq_lens[b];
+  int bad = 0;
+  if (seq_len < 0 || seq_len > p.max_seq_len) {
+    bad = 1;
+    if (threadIdx.x == 0 && split == 0 && j == 0) flag_error(p.err_flag, kFlagBadSeqLen);
+  }
+  const int t_begin = split * p.tokens_per_split;
+  const int t_end = bad ? t_begin : min(seq_len, t_begin + p.tokens_per_split);
+  if (!bad && t_end > t_begin) {
+    const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
+    const int k1 = (t_end - 1) >> p.log2_block_size;
+    for (int k = (t_begin >> p.log2_block_size) + threadIdx.x; k <= k1; k += blockDim.x) {
+      const int id = bt[k];
+      if (id < 0 || id >= p.num_blocks) {
+        bad = 1;
+        flag_error(p.err_flag, kFlagBadBlock);
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kW);
+    }
+    mbar_init(done_bar, kW);
+    mbar_init(merge_bar, kW);
+    fence_barrier_init();
+  }
+  bad = __syncthreads_or(bad);
+
+  const size_t row0 = static_cast<size_t>(b) * p.h_q + static_cast<size_t>(j) * G;
+  if (bad || t_end <= t_begin) {
+    // Bad data: zeros plus the poison marker.  Empty range: zeros, lse = -inf.
+    for (int e = threadIdx.x; e < G * kHeadDim; e += blockDim.x) {
+      const int r = e / kHeadDim, d = e % kHeadDim;
+      if (p.n_split == 1) {
+        static_cast<uint16_t*>(p.out)[(row0 + r) * kHeadDim + d] = 0;
+      } else {
+        p.part_o[((row0 + r) * p.n_split + split) * kHeadDim + d] = 0.f;
+        if (d == 0) p.part_lse[(row0 + r) * p.n_split + split] = bad ? DECATTN_POISON_LSE : kNegInf;
+      }
+    }
+    return;
+  }
+
+  const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
+  const int bs = p.block_size;
+
+  if (warp == 0) {
+    // ---------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint64_t policy = policy_evict_first();
+      const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
+      const int x0 = j * kHeadDim;
+      int issued = 0;
+      for (int it = 0; it < n_tiles; ++it) {
+        const int s = it % kStages;
+        if (!mbar_wait(empty0 + 8 * s, ((it / kStages) & 1) ^ 1, p.err_flag)) break;
+        const int t0 = t_begin + it * kTile;
+        const int nval = min(kTile, t_end - t0);
+        const uint32_t st = smem_u32(smem + s * kStageBytes);
+        const uint32_t fb = full0 + 8 * s;
+        if (bs >= kTile) {
+          const int row = bt[t0 >> p.log2_block_size] * bs + (t0 & (bs - 1));
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          tma_load_2d_hint(st, &tm_k, x0, row, fb, policy);
+          tma_load_2d_hint(st + kHalfBytes, &tm_k, x0 + 64, row, fb, policy);
+          tma_load_2d_hint(st + kKvTileBytes, &tm_v, x0, row, fb, policy);
+          tma_load_2d_hint(st + kKvTileBytes + kHalfBytes, &tm_v, x0 + 64, row, fb, policy);
+        } else {
+          const int nblk = (nval + bs - 1) >> p.log2_block_size;
+          const int box = bs * 128;
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nblk * 4 * box));
+          for (int k = 0; k < nblk; ++k) {
+            const int row = bt[(t0 >> p.log2_block_size) + k] * bs;
+            const uint32_t off = static_cast<uint32_t>(k * box);
+            tma_load_2d_hint(st + off, &tm_k, x0, row, fb, policy);
+            tma_load_2d_hint(st + kHalfBytes + off, &tm_k, x0 + 64, row, fb, policy);
+            tma_load_2d_hint(st + kKvTileBytes + off, &tm_v, x0, row, fb, policy);
+            tma_load_2d_hint(st + kKvTileBytes + kHalfBytes + off, &tm_v, x0 + 64, row, fb, policy);
+          }
+        }
+        ++issued;
+      }
+      // Never leave the CTA with copies in flight: wait (bounded) for the
+      // last phase of every stage that was filled.
+      for (int it = max(0, issued - kStages); it < issued; ++it)
+        if (!mbar_wait(full0 + 8 * (it % kStages), (it / kStages) & 1, p.err_flag)) break;
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int cw = warp - 1;
+  Consumer c;
+  c.init(p, b, j, cw, lane);
+  bool ok = true;
+  for (int it = 0; it < n_tiles; ++it) {
+    const int s = it % kStages;
+    if (!mbar_wait(full0 + 8 * s, (it / kStages) & 1, p.err_flag)) {
+      ok = false;
+      break;
+    }
+    const int nval = min(kTile, t_end - (t_begin + it * kTile));
+    c.tile(smem + s * kStageBytes, nval, p.scale_log2);
+    fence_proxy_async_smem();  // order any generic smem writes before the next TMA fill
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+  }
+
+  // Merge the consumer warps' (m, l, o) through shared memory (the ring is
+  // free once every warp has passed the last tile).
+  __syncwarp();
+  if (lane == 0) mbar_arrive(done_bar);
+  if (!ok || !mbar_wait(done_bar, 0, p.err_flag)) return;
+  float* mo = reinterpret_cast<float*>(smem);
+  float* mm = mo + kW * Consumer::kRowsPerWarp * kHeadDim;
+  float* ml = mm + kW * Consumer::kRowsPerWarp;
+  c.finish(mo, mm, ml, lane);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(merge_bar);
+  if (!mbar_wait(merge_bar, 0, p.err_flag)) return;
+
+  const int tid = threadIdx.x - 32;
+  for (int e = tid; e < G * kHeadDim; e += kW * 32) {
+    const int r = e / kHeadDim, d = e % kHeadDim;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kW; ++w)
+      if (Consumer::covers(w, r)) M = fmaxf(M, mm[Consumer::slot(w, r)]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+      if (!Consumer::covers(w, r)) continue;
+      const int sl = Consumer::slot(w, r);
+      const float mw = mm[sl];
+      if (mw == kNegInf) continue;
+      const float f = ex2(mw - M);
+      L = fmaf(ml[sl], f, L);
+      O = fmaf(mo[sl * kHeadDim + d], f, O);
+    }
+    const float res = L > 0.f ? O / L : 0.f;
+    if (p.n_split == 1) {
+      static_cast<uint16_t*>(p.out)[(row0 + r) * kHeadDim + d] = round1<kBF16>(res);
+    } else {
+      p.part_o[((row0 + r) * p.n_split + split) * kHeadDim + d] = res;
+      if (d == 0) p.part_lse[(row0 + r) * p.n_split + split] = L > 0.f ? M + lg2(L) : kNegInf;
+    }
+  }
+}
+
+template <class Consumer, bool kBF16, int kStages>
+cudaError_t launch_one(const GqaParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                       cudaStream_t stream) {
+  auto kern = gqa_partial_kernel<Consumer, kBF16, kStages>;
+  constexpr int smem = smem_bytes<Consumer, kStages>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_split, p.h_kv, p.batch);
+  kern<<<grid, 32 * (1 + Consumer::kWarps), smem, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <bool kBF16>
+cudaError_t dispatch(const GqaParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                     cudaStream_t stream) {
+  constexpr int S = 3;
+  switch (p.group) {
+    case 1: return launch_one<CcConsumer<1, kBF16>, kBF16, S>(p, tk, tv, stream);
+    case 2: return launch_one<CcConsumer<2, kBF16>, kBF16, S>(p, tk, tv, stream);
+    case 3: return launch_one<CcConsumer<3, kBF16>, kBF16, S>(p, tk, tv, stream);
+    case 4: return launch_one<CcConsumer<4, kBF16>, kBF16, S>(p, tk, tv, stream);
+    default: break;
+  }
+  if (p.group <= 16) return launch_one<MmaConsumer<1, kBF16>, kBF16, S>(p, tk, tv, stream);
+  if (p.group <= 32) return launch_one<MmaConsumer<2, kBF16>, kBF16, S>(p, tk, tv, stream);
+  return launch_one<MmaConsumer<4, kBF16>, kBF16, S>(p, tk, tv, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gqa_partial(const GqaParams& p, const CUtensorMap& tm_k,
+                               const CUtensorMap& tm_v, bool bf16, int /*num_sms*/,
+                               cudaStream_t stream) {
+  return bf16 ? dispatch<true>(p, tm_k, tm_v, stream) : dispatch<false>(p, tm_k, tm_v, stream);
+}
+
+}  // namespace decattn

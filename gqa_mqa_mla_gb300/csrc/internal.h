@@ -1,0 +1,71 @@
+// internal.h -- parameter blocks and launcher entry points shared between the
+// C-ABI front end (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace decattn {
+
+constexpr int kHeadDim = 128;      // GQA head dimension supported
+constexpr int kTile = 64;          // tokens per pipeline stage
+constexpr int kMlaHeads = 128;     // MLA query heads
+constexpr int kMlaDc = 512;        // MLA latent width
+constexpr int kMlaDr = 64;         // MLA decoupled-RoPE width
+constexpr int kMlaWidth = kMlaDc + kMlaDr;
+
+// Marker written into a partial log-sum-exp when the rows it covers met bad
+// data (bad block id or seq_len): the combine then writes zeros.
+#define DECATTN_POISON_LSE (__builtin_huge_valf())  // +inf
+
+struct GqaParams {
+  const void* q;              // [B, h_q, 128]
+  const int32_t* block_table; // [B, max_blocks_per_seq]
+  const int32_t* seq_lens;    // [B]
+  void* out;                  // [B, h_q, 128]      (written when n_split == 1)
+  float* part_o;              // [B, h_q, n_split, 128]
+  float* part_lse;            // [B, h_q, n_split]  log2 domain
+  int* err_flag;
+  int batch, h_q, h_kv, group;
+  int block_size, log2_block_size, num_blocks, max_blocks_per_seq, max_seq_len;
+  int n_split, tokens_per_split;  // tokens_per_split is a multiple of kTile
+  float scale_log2;               // scale * log2(e)
+};
+
+struct MlaParams {
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  void* out;                  // [B, 128, 512]  (written when n_split == 1)
+  float* part_o;              // [B, 128, n_split, 512]
+  float* part_lse;            // [B, 128, n_split]  log2 domain
+  int* err_flag;
+  int batch;
+  int block_size, log2_block_size, num_blocks, max_blocks_per_seq, max_seq_len;
+  int n_split, tokens_per_split;
+  float scale_log2;
+};
+
+struct CombineParams {
+  const float* part_o;
+  const float* part_lse;
+  void* out;
+  int rows;      // B * heads
+  int n_split;
+};
+
+// Kernel launchers (return cudaGetLastError() after the launch).
+cudaError_t launch_gqa_partial(const GqaParams& p, const CUtensorMap& tm_k,
+                               const CUtensorMap& tm_v, bool bf16, int num_sms,
+                               cudaStream_t stream);
+cudaError_t launch_mla_partial(const MlaParams& p, const CUtensorMap& tm_qa,
+                               const CUtensorMap& tm_qr, const CUtensorMap& tm_c, bool bf16,
+                               cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int d, bool bf16, cudaStream_t stream);
+
+// Planner shared by the front end and the workspace query.
+int plan_gqa_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms);
+int plan_mla_splits(int batch, int max_seq_len, int num_sms);
+
+}  // namespace decattn

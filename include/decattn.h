@@ -1,0 +1,170 @@
+/*
+ * decattn.h -- C ABI of libdecattn: single-token decode attention over a
+ * paged KV cache on one GB300 (sm_103a) GPU.
+ *
+ * Two operations:
+ *
+ *   gqa_decode  MHA / GQA / MQA.  h_q query heads share h_kv K/V heads;
+ *               query head i reads KV head i / (h_q / h_kv) by index
+ *               arithmetic, never by copying ("MQA, GQA, and MLA",
+ *               section 2 "The three answers" and section 8 "Implementation
+ *               notes", GQA in the kernel).  MHA is h_kv = h_q, MQA h_kv = 1.
+ *
+ *   mla_decode  Multi-head latent attention in its absorbed form: the 128
+ *               query heads arrive already multiplied by W_uk (q_absorbed,
+ *               512-d) plus a 64-d decoupled-RoPE query; each is scored
+ *               against the cached 512-d latent and the cached 64-d RoPE
+ *               key, and the latent itself serves as the value ("MQA, GQA,
+ *               and MLA", section 5 "MLA, mechanically", KEY TRICK; "Why
+ *               GQA's KV Cache Savings Don't Fully Reduce TPOT", "What Makes
+ *               MLA Different": 512 + 64 = 576 cached elements per token).
+ *
+ * For each sequence b and query head i the result is
+ *     s_t   = scale * (q_i . k_t)                  for t < seq_lens[b]
+ *     p     = softmax(s)  (base e)
+ *     out_i = sum_t p_t v_t
+ * where k_t / v_t come from the paged cache: token t of sequence b lives in
+ * physical block block_table[b][t / block_size], slot t % block_size.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *   contiguous, 16-byte aligned.  The library allocates nothing on the call
+ *   path; the split-KV workspace is caller-provided (see *_workspace_size).
+ * - Calls are asynchronous on launch->stream and return once the kernels are
+ *   enqueued.
+ * - A negative return is an error: host-side argument checks fail before
+ *   anything is launched; DECATTN_ERR_CUDA reports a launch failure.
+ * - Bad DATA found on the device (a block id outside [0, num_blocks), a
+ *   seq_len outside [0, max_seq_len]) never traps: the kernel ORs a
+ *   DECATTN_FLAG_* bit into *launch->err_flag (when non-NULL) and writes
+ *   zeros to the affected output rows.  The caller reads the flag after
+ *   synchronising.
+ * - seq_lens[b] = 0 gives an all-zero output row (an empty softmax).
+ * - Cache slots past seq_lens[b] inside a sequence's last block, and block
+ *   table entries past its last block, are never read.
+ */
+#ifndef DECATTN_H
+#define DECATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DECATTN_OK = 0,
+  DECATTN_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer, ... */
+  DECATTN_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. d_head != 128) */
+  DECATTN_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required   */
+  DECATTN_ERR_CUDA = -4         /* a CUDA call or kernel launch failed           */
+} decattn_status;
+
+typedef enum { DECATTN_FP16 = 0, DECATTN_BF16 = 1 } decattn_dtype;
+
+/* Bits ORed into *err_flag by the kernels. */
+#define DECATTN_FLAG_BAD_BLOCK 1   /* a block id outside [0, num_blocks)          */
+#define DECATTN_FLAG_BAD_SEQ_LEN 2 /* seq_lens[b] < 0 or > max_seq_len            */
+#define DECATTN_FLAG_TIMEOUT 4     /* a pipeline wait gave up (internal error)    */
+
+/* Largest split count accepted (num_splits) and chosen by the planner. */
+#define DECATTN_MAX_SPLITS 256
+
+/*
+ * Launch description shared by both operations.
+ *   batch              number of sequences B (>= 1)
+ *   num_blocks         physical blocks in the cache tensors (>= 1)
+ *   block_size         tokens per block (GQA: 8..256 power of two;
+ *                      MLA: 8, 16, 32 or 64)
+ *   max_blocks_per_seq row length of block_table
+ *   max_seq_len        host upper bound on seq_lens[] (sizes the split grid;
+ *                      must be <= max_blocks_per_seq * block_size)
+ *   num_splits         split-KV chunks per sequence; 0 = automatic
+ *   dtype              element type of every 16-bit tensor (decattn_dtype)
+ *   workspace          device scratch of workspace_bytes bytes (may be NULL
+ *                      when the required size is 0)
+ *   err_flag           device int receiving DECATTN_FLAG_* bits, or NULL
+ *   stream             cudaStream_t to launch on (NULL = legacy default)
+ */
+typedef struct {
+  int batch;
+  int num_blocks;
+  int block_size;
+  int max_blocks_per_seq;
+  int max_seq_len;
+  int num_splits;
+  int dtype;
+  void* workspace;
+  size_t workspace_bytes;
+  int* err_flag;
+  void* stream;
+} decattn_launch;
+
+/*
+ * gqa_decode -- MHA / GQA / MQA decode attention, one query token per
+ * sequence ("MQA, GQA, and MLA", sections 2, 4 and 8).
+ *   q            [batch, h_q, d_head]                       fp16/bf16
+ *   k_cache      [num_blocks, block_size, h_kv, d_head]     fp16/bf16
+ *   v_cache      [num_blocks, block_size, h_kv, d_head]     fp16/bf16
+ *   block_table  [batch, max_blocks_per_seq]                int32
+ *   seq_lens     [batch]                                    int32
+ *   out          [batch, h_q, d_head]                       fp16/bf16 (written)
+ *   h_q, h_kv    query / KV heads; h_q % h_kv == 0, h_q / h_kv <= 64
+ *   d_head       head dimension (128)
+ *   scale        softmax scale (typically 1/sqrt(d_head))
+ * Softmax and accumulation run in fp32; out is rounded to nearest-even.
+ */
+int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_table, const int32_t* seq_lens, void* out, int h_q, int h_kv,
+               int d_head, float scale, const decattn_launch* launch);
+
+/*
+ * mla_decode -- absorbed multi-head latent attention decode ("MQA, GQA, and
+ * MLA", section 5; "Why GQA's KV Cache Savings Don't Fully Reduce TPOT",
+ * "What Makes MLA Different").  128 heads, d_c = 512, d_rope = 64.
+ *   q_absorbed   [batch, 128, 512]   query times W_uk^(i), per head  fp16/bf16
+ *   q_rope       [batch, 128, 64]    decoupled-RoPE query (rotated)   fp16/bf16
+ *   latent_cache [num_blocks, block_size, 576]: elements [0,512) are the
+ *                latent c_t, [512,576) the RoPE key shared by all heads
+ *   block_table  [batch, max_blocks_per_seq] int32, seq_lens [batch] int32
+ *   out          [batch, 128, 512]   sum_t p_t c_t (latent-space output;
+ *                W_uv is applied by the caller)                      fp16/bf16
+ *   scale        softmax scale (typically 1/sqrt(128 + 64))
+ * s_t = scale * (q_absorbed . c_t + q_rope . k_rope_t).
+ */
+int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_cache,
+               const int32_t* block_table, const int32_t* seq_lens, void* out, float scale,
+               const decattn_launch* launch);
+
+/* Split count the automatic planner picks (num_splits = 0).  num_sms <= 0
+ * queries the current device.  Returns >= 1, or a negative status. */
+int gqa_decode_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,
+                           int num_sms);
+int mla_decode_plan_splits(int batch, int max_seq_len, int num_sms);
+
+/* Workspace bytes needed for num_splits (>= 1) split-KV chunks: fp32 partial
+ * outputs and log-sum-exps.  0 when num_splits == 1.  Returns 0 for invalid
+ * arguments as well; pure host arithmetic, no CUDA call. */
+size_t gqa_decode_workspace_size(int batch, int h_q, int d_head, int num_splits);
+size_t mla_decode_workspace_size(int batch, int num_splits);
+
+/* KV-cache bytes per token: n_layers * n_kv * d_head * 2 (K and V) * bytes
+ * ("Why GQA's KV Cache Savings Don't Fully Reduce TPOT", "KV Cache Size by
+ * Attention Variant").  MLA: n_layers * (d_c + d_rope) * bytes ("MQA, GQA,
+ * and MLA", section 5 "CACHE SIZE COMPARISON").  Negative on bad input. */
+int64_t decattn_kv_bytes_per_token(int n_layers, int n_kv, int d_head, int bytes);
+int64_t decattn_mla_bytes_per_token(int n_layers, int d_c, int d_rope, int bytes);
+
+/* Static English text for a decattn_status value; never NULL. */
+const char* decattn_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int decattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECATTN_H */

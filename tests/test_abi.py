@@ -1,0 +1,149 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/decattn.h declares, and its host-side argument checks return
+the documented statuses before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from gqa_mqa_mla_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "decattn.h")
+
+FAKE = 0x100000  # an aligned address that is never dereferenced by the host checks
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"gqa_decode", "mla_decode", "decattn_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in decattn.h but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.decattn_version() >= 100
+    for st in (0, -1, -2, -3, -4, 7):
+        assert binding.status_string(st)
+
+
+GOLDEN = os.path.join(ROOT, "tests", "golden", "cache_sizes.txt")
+
+
+def test_library_cache_size_formulas_match_the_oracle_and_pages(lib):
+    with open(GOLDEN) as f:
+        rows = [l.split("|")[0].split() for l in f if l.strip() and not l.startswith("#")]
+    for tok in rows:
+        kind = tok[1]
+        n_layers, a, b, nbytes = (int(x) for x in tok[2:6])
+        if kind == "kv":
+            assert binding.kv_bytes_per_token(n_layers, a, b, nbytes) == \
+                oracle.kv_bytes_per_token(n_layers, a, b, nbytes)
+        else:
+            assert binding.mla_bytes_per_token(n_layers, a, b, nbytes) == \
+                oracle.mla_bytes_per_token(n_layers, a, b, nbytes)
+    assert binding.kv_bytes_per_token(80, 64, 128, 2) == 2_621_440
+    assert binding.mla_bytes_per_token(1, 512, 64, 1) == 576
+    assert binding.kv_bytes_per_token(-1, 1, 1, 1) < 0
+
+
+def test_workspace_sizes(lib):
+    assert binding.gqa_workspace_size(4, 32, 1) == 0
+    ws = binding.gqa_workspace_size(4, 32, 8)
+    assert ws >= 4 * 32 * 8 * 128 * 4 + 4 * 32 * 8 * 4
+    assert binding.mla_workspace_size(2, 3) >= 2 * 128 * 3 * 512 * 4 + 2 * 128 * 3 * 4
+    assert binding.gqa_workspace_size(4, 32, 0) == 0
+    assert binding.gqa_workspace_size(4, 32, binding.MAX_SPLITS + 1) == 0
+
+
+def test_planner_is_bounded_and_spreads_long_sequences(lib):
+    for B, h_q, h_kv, S in [(1, 64, 8, 131072), (4, 64, 8, 131072), (64, 64, 8, 8192),
+                            (16, 32, 32, 4096), (2, 8, 2, 256), (1, 8, 8, 0)]:
+        ns = binding.gqa_plan_splits(B, h_q, h_kv, S, num_sms=152)
+        assert 1 <= ns <= binding.MAX_SPLITS
+        assert ns <= max(1, -(-S // 64))
+    # one short-batch long sequence must be split across many CTAs
+    assert binding.gqa_plan_splits(1, 64, 8, 131072, num_sms=152) >= 16
+    assert 1 <= binding.mla_plan_splits(32, 8192, num_sms=152) <= binding.MAX_SPLITS
+    assert binding.mla_plan_splits(1, 65536, num_sms=152) >= 16
+
+
+def _launch(**kw):
+    d = dict(batch=2, num_blocks=64, block_size=16, max_blocks_per_seq=16, max_seq_len=256,
+             num_splits=1, dtype=binding.DECATTN_BF16, workspace=None, workspace_bytes=0,
+             err_flag=None, stream=None)
+    d.update(kw)
+    return binding.Launch(**d)
+
+
+def _gqa(lib, L, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, out=FAKE, h_q=8, h_kv=2, d=128,
+         scale=0.088):
+    return lib.gqa_decode(q, k, v, bt, sl, out, h_q, h_kv, d, scale,
+                          None if L is None else ctypes.byref(L))
+
+
+def _mla(lib, L, qa=FAKE, qr=FAKE, c=FAKE, bt=FAKE, sl=FAKE, out=FAKE, scale=0.07):
+    return lib.mla_decode(qa, qr, c, bt, sl, out, scale, None if L is None else ctypes.byref(L))
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(L=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(q=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(k=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(out=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(h_q=9, h_kv=2), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(h_kv=0), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(d=64), binding.DECATTN_ERR_UNSUPPORTED),
+    (dict(h_q=256, h_kv=2), binding.DECATTN_ERR_UNSUPPORTED),
+    (dict(q=FAKE + 2), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(bt=FAKE + 2), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(batch=0)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(dtype=5)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(block_size=12)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(block_size=4)), binding.DECATTN_ERR_UNSUPPORTED),
+    (dict(L=dict(max_seq_len=257)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(num_splits=-1)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(num_splits=binding.MAX_SPLITS + 1)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(num_splits=4)), binding.DECATTN_ERR_WORKSPACE),
+    (dict(L=dict(num_splits=4, workspace=FAKE, workspace_bytes=100)),
+     binding.DECATTN_ERR_WORKSPACE),
+    (dict(L=dict(workspace=FAKE + 4)), binding.DECATTN_ERR_INVALID_ARG),
+])
+def test_gqa_host_checks(lib, case, expect):
+    case = dict(case)
+    L = case.pop("L", {})
+    L = None if L is None else _launch(**L)
+    assert _gqa(lib, L, **case) == expect
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(L=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(qa=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(c=FAKE + 8), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(block_size=128, max_blocks_per_seq=4)), binding.DECATTN_ERR_UNSUPPORTED),
+    (dict(L=dict(max_seq_len=10**6)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(num_splits=2)), binding.DECATTN_ERR_WORKSPACE),
+])
+def test_mla_host_checks(lib, case, expect):
+    case = dict(case)
+    L = case.pop("L", {})
+    L = None if L is None else _launch(**L)
+    assert _mla(lib, L, **case) == expect
