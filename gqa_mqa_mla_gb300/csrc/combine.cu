@@ -7,7 +7,9 @@
 // an empty range (lse = -inf) has weight 0.  A +inf lse marks a range that
 // met bad data: the whole row is written as zeros.
 //
-// One warp per row; lane l owns the float4 columns l, l + 32, ... of the row.
+// One CTA of kWarps warps per row.  Warp w accumulates the splits
+// j = w, w + kWarps, ... (lane l owns the float4 columns l, l + 32, ...), with
+// several splits' loads in flight; the warps' sums meet in shared memory.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -16,13 +18,14 @@ namespace {
 
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kPosInf = __builtin_huge_valf();
+constexpr int kWarps = 4;
 
 template <int D, bool kBF16>
-__global__ void __launch_bounds__(256) lse_combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(kWarps * 32) lse_combine_kernel(const CombineParams p) {
   constexpr int kVec = D / 128;  // float4 per lane
+  __shared__ float4 red[kWarps][D / 4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (row >= p.rows) return;
+  const int row = blockIdx.x;
   const int ns = p.n_split;
   const float* lse = p.part_lse + static_cast<size_t>(row) * ns;
 
@@ -39,11 +42,8 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(const CombineParams p)
 
   uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<size_t>(row) * D;
   if (poison || mx == kNegInf) {
-#pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-      uint2 z = make_uint2(0, 0);
-      *reinterpret_cast<uint2*>(out + (v * 32 + lane) * 4) = z;
-    }
+    for (int c = threadIdx.x; c < D / 4; c += kWarps * 32)
+      *reinterpret_cast<uint2*>(out + c * 4) = make_uint2(0, 0);
     return;
   }
 
@@ -57,10 +57,8 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(const CombineParams p)
   for (int v = 0; v < kVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* po = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * ns * D);
 #pragma unroll 4
-  for (int s = 0; s < ns; ++s) {
-    const float ls = lse[s];
-    if (ls == kNegInf) continue;
-    const float w = ex2(ls - mx);
+  for (int s = warp; s < ns; s += kWarps) {
+    const float w = ex2(lse[s] - mx);  // 0 for an empty split
 #pragma unroll
     for (int v = 0; v < kVec; ++v) {
       const float4 x = po[static_cast<size_t>(s) * (D / 4) + v * 32 + lane];
@@ -70,21 +68,27 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(const CombineParams p)
       acc[v].w = fmaf(w, x.w, acc[v].w);
     }
   }
-  const float inv = 1.f / wsum;
 #pragma unroll
-  for (int v = 0; v < kVec; ++v) {
+  for (int v = 0; v < kVec; ++v) red[warp][v * 32 + lane] = acc[v];
+  __syncthreads();
+  const float inv = 1.f / wsum;
+  for (int c = threadIdx.x; c < D / 4; c += kWarps * 32) {
+    float4 t = red[0][c];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) {
+      const float4 u = red[w][c];
+      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+    }
     uint2 w2;
-    w2.x = pack2<kBF16>(acc[v].x * inv, acc[v].y * inv);
-    w2.y = pack2<kBF16>(acc[v].z * inv, acc[v].w * inv);
-    *reinterpret_cast<uint2*>(out + (v * 32 + lane) * 4) = w2;
+    w2.x = pack2<kBF16>(t.x * inv, t.y * inv);
+    w2.y = pack2<kBF16>(t.z * inv, t.w * inv);
+    *reinterpret_cast<uint2*>(out + c * 4) = w2;
   }
 }
 
 template <int D, bool kBF16>
 cudaError_t launch_d(const CombineParams& p, cudaStream_t stream) {
-  constexpr int kWarps = 8;
-  const int blocks = (p.rows + kWarps - 1) / kWarps;
-  lse_combine_kernel<D, kBF16><<<blocks, kWarps * 32, 0, stream>>>(p);
+  lse_combine_kernel<D, kBF16><<<p.rows, kWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
