@@ -306,7 +306,7 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
   if (!make_map_2d(&tqa, q_absorbed, bf16, kMlaDc, q_rows, kMlaDc * 2, 64, kMlaHeads) ||
       !make_map_2d(&tqr, q_rope, bf16, kMlaDr, q_rows, kMlaDr * 2, 64, kMlaHeads) ||
       !make_map_2d(&tc, latent_cache, bf16, kMlaWidth, c_rows, kMlaWidth * 2, 64,
-                   static_cast<uint32_t>(L->block_size)))
+                   static_cast<uint32_t>(L->block_size < 32 ? L->block_size : 32)))
     return DECATTN_ERR_CUDA;
 
   cudaStream_t stream = static_cast<cudaStream_t>(L->stream);

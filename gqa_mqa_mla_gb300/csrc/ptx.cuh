@@ -108,6 +108,29 @@ DECATTN_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* err_flag) {
   return true;
 }
 
+// Bounded wait that also gives up as soon as another thread of the CTA has
+// raised the shared abort word (after its own wait timed out).
+DECATTN_DEV bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, int* err_flag,
+                                    volatile int* abort, bool cluster_scope = false) {
+  auto probe = [&]() {
+    return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (probe()) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t spins = 0;
+  while (!probe()) {
+    if ((++spins & 255u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        flag_error(err_flag, kFlagTimeout);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
 DECATTN_DEV bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* err_flag) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
