@@ -121,6 +121,31 @@ int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
                int d_head, float scale, const decattn_launch* launch);
 
 /*
+ * gqa_decode_noalloc -- gqa_decode for callers that may not allocate device
+ * memory.  The pages have no counterpart: this is an interface convenience.
+ *
+ * Same arguments, results and statuses as gqa_decode, except that
+ * launch->workspace / workspace_bytes are ignored: the split-KV scratch is a
+ * fixed 8 MiB (8 * 2^20 bytes) device array inside the library, held by every
+ * GPU that loads it until the process exits.  Meant for hosts that cannot
+ * call cudaMalloc around a decode call (engines that reserve all free HBM for
+ * the KV cache, runtime plugin interfaces that hand over only inputs and
+ * outputs, loops that must not pay an allocation's synchronisation).
+ *   - A split plan needing more than 8 MiB of scratch returns
+ *     DECATTN_ERR_WORKSPACE and launches nothing (the need is
+ *     gqa_decode_workspace_size(batch, h_q, d_head, splits)).
+ *   - All calls on a device share the array: calls that may overlap on the
+ *     GPU (unordered streams) race; serialise them.
+ *   - The first call on a device looks up the array's address with that
+ *     device current; make it before any stream capture.
+ *   - Nothing in the array needs to start at zero; its contents after a call
+ *     are unspecified.
+ */
+int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* seq_lens, void* out, int h_q,
+                       int h_kv, int d_head, float scale, const decattn_launch* launch);
+
+/*
  * mla_decode -- absorbed multi-head latent attention decode ("MQA, GQA, and
  * MLA", section 5; "Why GQA's KV Cache Savings Don't Fully Reduce TPOT",
  * "What Makes MLA Different").  128 heads, d_c = 512, d_rope = 64.
