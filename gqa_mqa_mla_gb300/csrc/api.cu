@@ -105,8 +105,27 @@ int plan_gqa_splits(int batch, int /*h_q*/, int h_kv, int max_seq_len, int num_s
 }
 
 int plan_mla_splits(int batch, int max_seq_len, int num_sms) {
-  // MLA partial kernel: one CTA pair per two SMs.
-  return plan_splits(batch, max_seq_len, num_sms / 2);
+  // MLA partial kernel: one CTA pair per two SMs, one pair resident per SM
+  // pair.  Each split pays a fixed start (Q load, TMEM allocation, pipeline
+  // fill) and end (a 128 x 512 fp32 partial), about four 64-token tiles, so
+  // choose the split count minimising waves x (tiles per split + 4).
+  const int slots = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  const int tiles = max_seq_len > 0 ? (max_seq_len + kTile - 1) / kTile : 1;
+  int best = 1;
+  double best_cost = 1e300;
+  const int cap = tiles < DECATTN_MAX_SPLITS ? tiles : DECATTN_MAX_SPLITS;
+  for (int ns = 1; ns <= cap; ++ns) {
+    int tps = 0;
+    if (resolve_splits(max_seq_len, ns, &tps) != ns) continue;
+    const long long ctas = static_cast<long long>(batch) * ns;
+    const double waves = static_cast<double>((ctas + slots - 1) / slots);
+    const double cost = waves * (tps / kTile + 4.0);
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = ns;
+    }
+  }
+  return best;
 }
 
 }  // namespace decattn
@@ -300,17 +319,18 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
   }
 
   const bool bf16 = L->dtype == DECATTN_BF16;
-  const uint64_t q_rows = static_cast<uint64_t>(L->batch) * kMlaHeads;
   const uint64_t c_rows = static_cast<uint64_t>(L->num_blocks) * L->block_size;
-  CUtensorMap tqa, tqr, tc;
+  const uint64_t q_rows = static_cast<uint64_t>(L->batch) * kMlaHeads;
+  CUtensorMap tqa, tc;
   if (!make_map_2d(&tqa, q_absorbed, bf16, kMlaDc, q_rows, kMlaDc * 2, 64, kMlaHeads) ||
-      !make_map_2d(&tqr, q_rope, bf16, kMlaDr, q_rows, kMlaDr * 2, 64, kMlaHeads) ||
       !make_map_2d(&tc, latent_cache, bf16, kMlaWidth, c_rows, kMlaWidth * 2, 64,
                    static_cast<uint32_t>(L->block_size < 32 ? L->block_size : 32)))
     return DECATTN_ERR_CUDA;
+  p.q_abs = q_absorbed;
+  p.q_rope = q_rope;
 
   cudaStream_t stream = static_cast<cudaStream_t>(L->stream);
-  cudaError_t e = launch_mla_partial(p, tqa, tqr, tc, bf16, stream);
+  cudaError_t e = launch_mla_partial(p, tqa, tc, bf16, stream);
   if (e == cudaErrorNotSupported) return DECATTN_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DECATTN_ERR_CUDA;
   if (eff > 1) {

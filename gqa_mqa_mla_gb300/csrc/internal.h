@@ -35,6 +35,8 @@ struct GqaParams {
 };
 
 struct MlaParams {
+  const void* q_abs;          // [B, 128, 512]
+  const void* q_rope;         // [B, 128, 64]
   const int32_t* block_table;
   const int32_t* seq_lens;
   void* out;                  // [B, 128, 512]  (written when n_split == 1)
@@ -60,8 +62,7 @@ cudaError_t launch_gqa_partial(const GqaParams& p, const CUtensorMap& tm_k,
                                const CUtensorMap& tm_v, bool bf16, int num_sms,
                                cudaStream_t stream);
 cudaError_t launch_mla_partial(const MlaParams& p, const CUtensorMap& tm_qa,
-                               const CUtensorMap& tm_qr, const CUtensorMap& tm_c, bool bf16,
-                               cudaStream_t stream);
+                               const CUtensorMap& tm_c, bool bf16, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int d, bool bf16, cudaStream_t stream);
 
 // Planner shared by the front end and the workspace query.

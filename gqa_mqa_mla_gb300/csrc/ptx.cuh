@@ -288,6 +288,25 @@ DECATTN_DEV void cluster_sync() {
                    : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into
+// another CTA's shared memory; completion is counted in bytes on the
+// destination CTA's mbarrier (both destination addresses from mapa).
+DECATTN_DEV void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                   uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+// Plain 16-byte store into another CTA's shared memory (shared::cluster address).
+DECATTN_DEV void st_cluster_v4(uint32_t remote_addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote_addr), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 // Asynchronous 16-byte store into another CTA's shared memory, completing
 // `bytes`-counted transactions on that CTA's mbarrier.
 DECATTN_DEV void st_async_v4(uint32_t remote_addr, uint32_t remote_bar, float a, float b, float c,
@@ -331,6 +350,29 @@ DECATTN_DEV void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, u
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16, one CTA.  A row i sits in TMEM
+// lane i, two 16-bit elements per 32-bit column (even k in the low half); a
+// K = 16 step reads 8 columns starting at a_tmem.
+DECATTN_DEV void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 16 columns of 32-bit into TMEM (thread t of the warp: lane base + t).
+DECATTN_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
       : "memory");
 }
 
