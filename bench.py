@@ -43,6 +43,8 @@ MLA_WORKLOAD = "deepseek_v2_mla_b32_s8k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GQA_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/gqa_decode.cu", "gqa_mqa_mla_gb300/csrc/ptx.cuh",
                       "gqa_mqa_mla_gb300/csrc/internal.h"]
+MLA_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/mla_decode.cu", "gqa_mqa_mla_gb300/csrc/ptx.cuh",
+                      "gqa_mqa_mla_gb300/csrc/internal.h"]
 
 
 # ----------------------------------------------------------------- algorithmic work
@@ -427,6 +429,7 @@ def main():
             tc = fl / (ms * 1e-3) / 1e12
             t_bw = part_bytes[name] / (hbm * 1e9)
             t_tc = fl / (peaks["bf16_tflops_sustained"] * 1e12)
+            d["traffic"] = load_traffic("mla_partial_deepseek_v2", MLA_KERNEL_SOURCES)
             d.update({"flops": fl, "TFLOPs": tc,
                       "frac_of_tensor_peak": tc / peaks["bf16_tflops_sustained"],
                       "frac_of_roofline": max(t_bw, t_tc) / (ms * 1e-3),
