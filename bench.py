@@ -96,6 +96,20 @@ def load_traffic(kernel: str, paths):
     return d.get("bytes_per_launch")
 
 
+def reduce_max(value: float, dist=None, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity without a process group)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(step_bytes_per_rank: int, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: every rank processes its own step_bytes per step."""
+    return world * step_bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -224,8 +238,8 @@ def run_reference(args, rank, world):
     budget = 120.0 / max(1, args.steps + args.warmup)
     per_unit = t1 + t2 / 8 if mx else t1
     units = max(1, int(budget / max(per_unit, 1e-6)))
-    gg = units if gx else 0
-    ms = max(1, units // 8) if mx else 0
+    gg = min(units, gx.batch * gx.h_kv) if gx else 0
+    ms = min(max(1, units // 8), mx.batch) if mx else 0
     times, nbytes = [], 0
     for s in range(args.warmup + args.steps):
         t, b, _ = oracle_sample(gx, mx, gg, ms, seed=s)
@@ -365,12 +379,9 @@ def main():
     part_ms = {name: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)) / K
                for i, (name, _) in enumerate(calls)}
     err = int(flag.item())
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = reduce_max(elapsed_ms, dist, dev)
     ms_per_step = elapsed_ms / K
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbps(step_bytes, ms_per_step, world)
 
     # ---------------- end to end through the public API from pinned host buffers
     e2e = None
@@ -407,12 +418,8 @@ def main():
             e2e_step()
         s1.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = s0.elapsed_time(s1) / n
-        if dist:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * step_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        e_ms = reduce_max(s0.elapsed_time(s1) / n, dist, dev)
+        e2e = {"value": whole_job_gbps(step_bytes, e_ms, world), "unit": "GB/s",
                "ms_per_step": e_ms, "steps": n, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
         err |= int(flag.item())
