@@ -39,21 +39,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D tensor map over a row-major [outer, inner] 16-bit tensor whose rows are
-// row_bytes apart; boxes of box_inner x box_outer elements, 128-byte swizzle.
-bool make_map_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint64_t outer,
-                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+// 2-D tensor map over a row-major [outer, inner] tensor of element type dt
+// whose rows are row_bytes apart; boxes of box_inner x box_outer elements,
+// 128-byte swizzle.
+bool make_map_2d_t(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner,
+                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// The same over a 16-bit (fp16 / bf16) tensor.
+bool make_map_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return make_map_2d_t(m, base,
+                       bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                       inner, outer, row_bytes, box_inner, box_outer);
 }
 
 int device_sm_count() {
@@ -105,27 +113,30 @@ int plan_gqa_splits(int batch, int /*h_q*/, int h_kv, int max_seq_len, int num_s
 }
 
 int plan_mla_splits(int batch, int max_seq_len, int num_sms) {
-  // MLA partial kernel: one CTA pair per two SMs, one pair resident per SM
-  // pair.  Each split pays a fixed start (Q load, TMEM allocation, pipeline
-  // fill) and end (a 128 x 512 fp32 partial), about four 64-token tiles, so
-  // choose the split count minimising waves x (tiles per split + 4).
-  const int slots = num_sms / 2 > 0 ? num_sms / 2 : 1;
-  const int tiles = max_seq_len > 0 ? (max_seq_len + kTile - 1) / kTile : 1;
-  int best = 1;
-  double best_cost = 1e300;
-  const int cap = tiles < DECATTN_MAX_SPLITS ? tiles : DECATTN_MAX_SPLITS;
-  for (int ns = 1; ns <= cap; ++ns) {
-    int tps = 0;
-    if (resolve_splits(max_seq_len, ns, &tps) != ns) continue;
-    const long long ctas = static_cast<long long>(batch) * ns;
-    const double waves = static_cast<double>((ctas + slots - 1) / slots);
-    const double cost = waves * (tps / kTile + 4.0);
-    if (cost < best_cost * 0.999) {
-      best_cost = cost;
-      best = ns;
-    }
-  }
-  return best;
+  // MLA partial kernel: one CTA pair per two SMs, all pairs resident at
+  // once, each streaming an equal share of the batch's 64-token tiles.  Use
+  // every SM pair, but give each pair at least two tiles of the host's
+  // upper bound (batch x tiles of max_seq_len) so that tiny batches do not
+  // pay a partial + combine for nothing.
+  const long long slots = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  const long long tiles =
+      static_cast<long long>(batch) * (max_seq_len > 0 ? (max_seq_len + kTile - 1) / kTile : 1);
+  long long pairs = tiles / 2;
+  if (pairs > slots) pairs = slots;
+  if (pairs > DECATTN_MAX_SPLITS) pairs = DECATTN_MAX_SPLITS;
+  return pairs < 1 ? 1 : static_cast<int>(pairs);
+}
+
+size_t mla_workspace_bytes(int batch, int n_pairs, size_t* off_lse, size_t* off_o) {
+  if (batch < 1 || n_pairs < 1 || n_pairs > DECATTN_MAX_SPLITS) return 0;
+  if (n_pairs == 1) return 0;
+  const size_t slots = 2 * static_cast<size_t>(n_pairs);
+  const size_t hdr = align_up((static_cast<size_t>(kHdrPref) + batch + 1) * sizeof(int));
+  const size_t lse = align_up(slots * kMlaHeads * sizeof(float));
+  const size_t o = align_up(slots * kMlaHeads * kMlaDc * sizeof(float));
+  if (off_lse) *off_lse = hdr;
+  if (off_o) *off_o = hdr + lse;
+  return hdr + lse + o;
 }
 
 }  // namespace decattn
@@ -166,7 +177,7 @@ size_t gqa_decode_workspace_size(int batch, int h_q, int d_head, int num_splits)
 }
 
 size_t mla_decode_workspace_size(int batch, int num_splits) {
-  return gqa_decode_workspace_size(batch, kMlaHeads, kMlaDc, num_splits);
+  return mla_workspace_bytes(batch, num_splits, nullptr, nullptr);
 }
 
 int gqa_decode_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,
@@ -286,14 +297,12 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
     return DECATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return DECATTN_ERR_INVALID_ARG;
 
-  int n_split = L->num_splits;
-  if (n_split == 0) {
+  int n_pairs = L->num_splits;
+  if (n_pairs == 0) {
     const int sms = device_sm_count();
     if (sms <= 0) return DECATTN_ERR_CUDA;
-    n_split = plan_mla_splits(L->batch, L->max_seq_len, sms);
+    n_pairs = plan_mla_splits(L->batch, L->max_seq_len, sms);
   }
-  int tps = 0;
-  const int eff = resolve_splits(L->max_seq_len, n_split, &tps);
 
   MlaParams p{};
   p.block_table = block_table;
@@ -306,36 +315,44 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
   p.num_blocks = L->num_blocks;
   p.max_blocks_per_seq = L->max_blocks_per_seq;
   p.max_seq_len = L->max_seq_len;
-  p.n_split = eff;
-  p.tokens_per_split = tps;
+  p.n_pairs = n_pairs;
   p.scale_log2 = scale * 1.4426950408889634f;
-  if (eff > 1) {
-    const size_t need = mla_decode_workspace_size(L->batch, eff);
+  if (n_pairs > 1) {
+    size_t off_lse = 0, off_o = 0;
+    const size_t need = mla_workspace_bytes(L->batch, n_pairs, &off_lse, &off_o);
     if (!L->workspace || L->workspace_bytes < need) return DECATTN_ERR_WORKSPACE;
-    const size_t rows = static_cast<size_t>(L->batch) * kMlaHeads * eff;
-    p.part_o = static_cast<float*>(L->workspace);
-    p.part_lse = reinterpret_cast<float*>(static_cast<char*>(L->workspace) +
-                                          align_up(rows * kMlaDc * sizeof(float)));
+    char* ws = static_cast<char*>(L->workspace);
+    p.ws_hdr = reinterpret_cast<int*>(ws);
+    p.part_lse = reinterpret_cast<float*>(ws + off_lse);
+    p.part_o = reinterpret_cast<float*>(ws + off_o);
   }
 
   const bool bf16 = L->dtype == DECATTN_BF16;
   const uint64_t c_rows = static_cast<uint64_t>(L->num_blocks) * L->block_size;
   const uint64_t q_rows = static_cast<uint64_t>(L->batch) * kMlaHeads;
-  CUtensorMap tqa, tc;
+  CUtensorMap tqa, tc, tout, tpo;
   if (!make_map_2d(&tqa, q_absorbed, bf16, kMlaDc, q_rows, kMlaDc * 2, 64, kMlaHeads) ||
       !make_map_2d(&tc, latent_cache, bf16, kMlaWidth, c_rows, kMlaWidth * 2, 64,
-                   static_cast<uint32_t>(L->block_size < 32 ? L->block_size : 32)))
+                   static_cast<uint32_t>(L->block_size < 32 ? L->block_size : 32)) ||
+      !make_map_2d(&tout, out, bf16, kMlaDc, q_rows, kMlaDc * 2, 64, kMlaHeads))
     return DECATTN_ERR_CUDA;
+  if (n_pairs > 1) {
+    if (!make_map_2d_t(&tpo, p.part_o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, kMlaDc,
+                       2ull * n_pairs * kMlaHeads, kMlaDc * 4, 32, kMlaHeads))
+      return DECATTN_ERR_CUDA;
+  } else {
+    tpo = tout;  // never used: every segment of a single pair is whole
+  }
   p.q_abs = q_absorbed;
   p.q_rope = q_rope;
 
   cudaStream_t stream = static_cast<cudaStream_t>(L->stream);
-  cudaError_t e = launch_mla_partial(p, tqa, tc, bf16, stream);
+  cudaError_t e = launch_mla_partial(p, tqa, tc, tout, tpo, bf16, stream);
   if (e == cudaErrorNotSupported) return DECATTN_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DECATTN_ERR_CUDA;
-  if (eff > 1) {
-    CombineParams c{p.part_o, p.part_lse, out, L->batch * kMlaHeads, eff};
-    if (launch_combine(c, kMlaDc, bf16, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
+  if (n_pairs > 1) {
+    MlaCombineParams c{p.part_o, p.part_lse, p.ws_hdr, out, L->batch, n_pairs};
+    if (launch_mla_combine(c, bf16, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
   }
   return DECATTN_OK;
 }

@@ -20,19 +20,18 @@ constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kPosInf = __builtin_huge_valf();
 constexpr int kWarps = 4;
 
-template <int D, bool kBF16>
-__global__ void __launch_bounds__(kWarps * 32) lse_combine_kernel(const CombineParams p) {
+// Merge ns partial rows into one output row.  Partial s has its lse at
+// lse[row(s)] and its D values at po[row(s) * D].
+template <int D, bool kBF16, typename RowOf>
+__device__ __forceinline__ void merge_row(const float* lse, const float* po, RowOf row, int ns,
+                                          uint16_t* out, float4 (*red)[D / 4]) {
   constexpr int kVec = D / 128;  // float4 per lane
-  __shared__ float4 red[kWarps][D / 4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x;
-  const int ns = p.n_split;
-  const float* lse = p.part_lse + static_cast<size_t>(row) * ns;
 
   float mx = kNegInf;
   bool poison = false;
   for (int s = lane; s < ns; s += 32) {
-    const float v = lse[s];
+    const float v = lse[row(s)];
     poison |= (v == kPosInf);
     mx = fmaxf(mx, v);
   }
@@ -40,7 +39,6 @@ __global__ void __launch_bounds__(kWarps * 32) lse_combine_kernel(const CombineP
   for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   poison = __any_sync(0xffffffffu, poison);
 
-  uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<size_t>(row) * D;
   if (poison || mx == kNegInf) {
     for (int c = threadIdx.x; c < D / 4; c += kWarps * 32)
       *reinterpret_cast<uint2*>(out + c * 4) = make_uint2(0, 0);
@@ -48,20 +46,20 @@ __global__ void __launch_bounds__(kWarps * 32) lse_combine_kernel(const CombineP
   }
 
   float wsum = 0.f;
-  for (int s = lane; s < ns; s += 32) wsum += ex2(lse[s] - mx);
+  for (int s = lane; s < ns; s += 32) wsum += ex2(lse[row(s)] - mx);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
 
   float4 acc[kVec];
 #pragma unroll
   for (int v = 0; v < kVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * ns * D);
+  const float4* po4 = reinterpret_cast<const float4*>(po);
 #pragma unroll 4
   for (int s = warp; s < ns; s += kWarps) {
-    const float w = ex2(lse[s] - mx);  // 0 for an empty split
+    const float w = ex2(lse[row(s)] - mx);  // 0 for an empty split
 #pragma unroll
     for (int v = 0; v < kVec; ++v) {
-      const float4 x = po[static_cast<size_t>(s) * (D / 4) + v * 32 + lane];
+      const float4 x = po4[row(s) * (D / 4) + v * 32 + lane];
       acc[v].x = fmaf(w, x.x, acc[v].x);
       acc[v].y = fmaf(w, x.y, acc[v].y);
       acc[v].z = fmaf(w, x.z, acc[v].z);
@@ -86,6 +84,43 @@ __global__ void __launch_bounds__(kWarps * 32) lse_combine_kernel(const CombineP
   }
 }
 
+// Per-sequence split-KV partials: row r's splits are contiguous.
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(kWarps * 32) lse_combine_kernel(const CombineParams p) {
+  __shared__ float4 red[kWarps][D / 4];
+  const size_t row0 = static_cast<size_t>(blockIdx.x) * p.n_split;
+  merge_row<D, kBF16>(p.part_lse, p.part_o, [row0](int s) { return row0 + s; }, p.n_split,
+                      static_cast<uint16_t*>(p.out) + static_cast<size_t>(blockIdx.x) * D, red);
+}
+
+// MLA partials of a balanced schedule: sequence b's tiles [g0, g1) were cut
+// by the pair slices [q T, q T + T).  Only the first and the last segment of
+// a slice can be partial, and pair q writes them to slots 2 q and 2 q + 1:
+// b's piece in its first pair q0 is slot 2 q0 + 1 unless b starts that
+// slice, and its piece in every later pair starts that pair's slice (slot
+// 2 q).  Rows of sequences that one pair covered whole (or that have no
+// tiles) were written by the partial kernel and are skipped.  One CTA per
+// (sequence, head).
+template <bool kBF16>
+__global__ void __launch_bounds__(kWarps * 32) mla_combine_kernel(const MlaCombineParams p) {
+  __shared__ float4 red[kWarps][kMlaDc / 4];
+  const int b = blockIdx.x / kMlaHeads, h = blockIdx.x % kMlaHeads;
+  const int T = p.ws_hdr[0];
+  const int g0 = p.ws_hdr[kHdrPref + b], g1 = p.ws_hdr[kHdrPref + b + 1];
+  if (g1 <= g0 || T < 1) return;
+  const int q0 = min(g0 / T, p.n_pairs - 1), q1 = min((g1 - 1) / T, p.n_pairs - 1);
+  if (q1 == q0) return;
+  const int first_slot = 2 * q0 + (g0 == q0 * T ? 0 : 1);
+  auto row = [=](int s) {
+    const int slot = s == 0 ? first_slot : 2 * (q0 + s);
+    return static_cast<size_t>(slot) * kMlaHeads + h;
+  };
+  merge_row<kMlaDc, kBF16>(p.part_lse, p.part_o, row, q1 - q0 + 1,
+                           static_cast<uint16_t*>(p.out) +
+                               (static_cast<size_t>(b) * kMlaHeads + h) * kMlaDc,
+                           red);
+}
+
 template <int D, bool kBF16>
 cudaError_t launch_d(const CombineParams& p, cudaStream_t stream) {
   lse_combine_kernel<D, kBF16><<<p.rows, kWarps * 32, 0, stream>>>(p);
@@ -93,6 +128,16 @@ cudaError_t launch_d(const CombineParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_mla_combine(const MlaCombineParams& p, bool bf16, cudaStream_t stream) {
+  if (p.batch <= 0) return cudaSuccess;
+  const int rows = p.batch * kMlaHeads;
+  if (bf16)
+    mla_combine_kernel<true><<<rows, kWarps * 32, 0, stream>>>(p);
+  else
+    mla_combine_kernel<false><<<rows, kWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const CombineParams& p, int d, bool bf16, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;

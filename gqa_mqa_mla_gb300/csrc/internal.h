@@ -34,19 +34,33 @@ struct GqaParams {
   float scale_log2;               // scale * log2(e)
 };
 
+// MLA workspace (n_pairs > 1): a header of kHdrPref ints (tiles per pair,
+// total tiles), the first-tile index of every sequence (batch + 1 ints),
+// then the partial log2-sum-exps and outputs of 2 n_pairs slots.
+constexpr int kHdrPref = 64;
+
 struct MlaParams {
   const void* q_abs;          // [B, 128, 512]
   const void* q_rope;         // [B, 128, 64]
   const int32_t* block_table;
   const int32_t* seq_lens;
-  void* out;                  // [B, 128, 512]  (written when n_split == 1)
-  float* part_o;              // [B, 128, n_split, 512]
-  float* part_lse;            // [B, 128, n_split]  log2 domain
+  void* out;                  // [B, 128, 512]
+  float* part_o;              // [slots, 128, 512]
+  float* part_lse;            // [slots, 128]  log2 domain
+  int* ws_hdr;                // header + first-tile table (null when n_pairs == 1)
   int* err_flag;
   int batch;
   int block_size, log2_block_size, num_blocks, max_blocks_per_seq, max_seq_len;
-  int n_split, tokens_per_split;
+  int n_pairs;                // CTA pairs sharing the batch's tiles
   float scale_log2;
+};
+
+struct MlaCombineParams {
+  const float* part_o;
+  const float* part_lse;
+  const int* ws_hdr;
+  void* out;
+  int batch, n_pairs;
 };
 
 struct CombineParams {
@@ -61,12 +75,17 @@ struct CombineParams {
 cudaError_t launch_gqa_partial(const GqaParams& p, const CUtensorMap& tm_k,
                                const CUtensorMap& tm_v, bool bf16, int num_sms,
                                cudaStream_t stream);
+// tm_out: 16-bit [B * 128, 512] output, boxes of 64 x 128; tm_po: fp32
+// [2 n_pairs * 128, 512] partials, boxes of 32 x 128 (both 128-byte swizzle).
 cudaError_t launch_mla_partial(const MlaParams& p, const CUtensorMap& tm_qa,
-                               const CUtensorMap& tm_c, bool bf16, cudaStream_t stream);
+                               const CUtensorMap& tm_c, const CUtensorMap& tm_out,
+                               const CUtensorMap& tm_po, bool bf16, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int d, bool bf16, cudaStream_t stream);
+cudaError_t launch_mla_combine(const MlaCombineParams& p, bool bf16, cudaStream_t stream);
 
 // Planner shared by the front end and the workspace query.
 int plan_gqa_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms);
 int plan_mla_splits(int batch, int max_seq_len, int num_sms);
+size_t mla_workspace_bytes(int batch, int n_pairs, size_t* off_lse, size_t* off_o);
 
 }  // namespace decattn

@@ -10,27 +10,28 @@
 // Both contractions are dense 128-row GEMM tiles: S = Q C^T (K = 576) and
 // O = P C_lat (N = 512).
 //
-// Work split: a cluster of two CTAs handles one (split, sequence).  The fp32
-// O accumulator for 128 heads x 512 columns would fill all of one SM's
-// tensor memory, so CTA r accumulates only O[:, 256 r : 256 r + 256].  Both
-// CTAs compute the full score tile S = Q C^T (the same MMA sequence on the
-// same bytes, hence the same bits) and the same online softmax, so they need
-// to exchange nothing; the cluster only co-schedules the pair so that the
-// second load of every cache tile is an L2 hit.  The redundant score GEMM
-// costs 1.44x the minimum tensor work, which at 576-d keys still balances
-// the HBM stream on GB300.
+// Work split: a cluster of two CTAs streams one share of the batch's tiles
+// (see the work schedule below).  The fp32 O accumulator for 128 heads x 512
+// columns would fill all of one SM's tensor memory, so CTA r accumulates only
+// O[:, 256 r : 256 r + 256].  Both CTAs compute the full score tile
+// S = Q C^T (the same MMA sequence on the same bytes, hence the same bits)
+// and the same online softmax, so they need to exchange nothing; the cluster
+// only co-schedules the pair so that the second load of every cache tile is
+// an L2 hit.  The redundant score GEMM costs 1.44x the minimum tensor work.
 //
-// Tile width: every tcgen05.mma costs at least ~60 SM cycles whatever its
-// N, and only N >= 128 reaches the full tensor rate (measured on GB300:
-// M = 128, K = 16 bf16 runs at ~1.1k / 2.2k / 3.9k MAC per cycle for N = 32 /
-// 64 / 128).  The score GEMM's N is the token count of a tile, so tiles are
-// 64 tokens, the widest that fits tensor memory next to O and Q.
+// Tile width: a chain of tcgen05.mma (M = 128, K = 16, bf16) into one
+// accumulator costs ~58 SM cycles per instruction for any N <= 64 and only
+// N >= 128 reaches the full tensor rate (measured on GB300: ~1.1k / 2.2k /
+// 3.9k MAC per cycle for N = 32 / 64 / 128).  The score GEMM's N is the
+// token count of a tile, so tiles are 64 tokens, the widest that fits tensor
+// memory next to O and Q.
 //
 // Operand placement (per CTA):
 //   Q[:, 0:256)    shared memory (TMA), 128-byte swizzled K-major      A of S
 //   Q[:, 256:576)  TMEM, 160 columns (two 16-bit values per column)  A of S
 //   cache tiles    shared memory ring, 2 stages x 64 tokens x 576     B of S, PV
 //   P(j)           TMEM, 32 columns                                  A of PV
+//   epilogue       the Q shared-memory region, once a segment's S are done
 // TMEM columns: O [0, 256) fp32 | Q [256, 416) | S [416, 480) | P [480, 512).
 //
 // Per CTA (320 threads):
@@ -95,17 +96,78 @@ enum : int {
   kBarQs = kBarPvDone + 1,                 // Q[:, 0:256) in shared memory (TMA)
   kBarMax = kBarQs + 1,                    // row tile maxima exchanged (256 arrivals)
   kBarSum = kBarMax + 1,                   // row sums exchanged (256 arrivals)
-  kBarDrain = kBarSum + 1,
+  kBarEpiW = kBarSum + 1,                  // epilogue round staged in smem (256 arrivals)
+  kBarEpiR = kBarEpiW + 1,                 // epilogue round's bulk stores have read smem
+  kBarEpiDone = kBarEpiR + 1,              // segment epilogue done: Q smem reusable
+  kBarDrain = kBarEpiDone + 1,
   kNumBars = kBarDrain + 1
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kTmemP + kT / 2 <= kTmemCols, "tensor memory columns");
 
+// Work schedule.  The batch's 64-token tiles, sequence after sequence, form
+// one list of T_all tiles (an invalid seq_len counts as 0 tiles); pair p of
+// the P CTA pairs takes the slice [p T, p T + T), T = ceil(T_all / P), so
+// every pair streams the same number of tiles however ragged the lengths
+// are.  The slice is cut at sequence boundaries into segments: a segment
+// holding a whole sequence writes its output rows directly; one holding
+// part of a sequence writes an fp32 partial (normalised O and log2-sum-exp)
+// that the combine merges.  Only a slice's first and last segments can be
+// partial; they go to workspace slots 2 p and 2 p + 1.  A sequence with no
+// tiles is zeroed by the pair whose slice contains its start.
+enum : int { kSegZero = 0, kSegDirect = 1, kSegPartial = 2 };
+
+struct Sched {
+  int pair, n_pairs, T, lo, hi;  // this pair's tile slice [lo, hi)
+};
+struct Cursor {
+  int b, pref;  // next sequence to examine and the index of its first tile
+};
+struct Seg {
+  int b, t0, t1, kind;  // tokens [t0, t1) of sequence b
+};
+
+__device__ __forceinline__ int seq_tiles(const MlaParams& p, int len) {
+  return (len < 0 || len > p.max_seq_len) ? 0 : (len + kT - 1) / kT;
+}
+
+// Next segment of this pair's slice (every role walks the same sequence).
+__device__ bool next_seg(const MlaParams& p, const Sched& sc, Cursor& cur, Seg& sg) {
+  while (cur.b < p.batch) {
+    const int b = cur.b, pref = cur.pref;
+    const int len = p.seq_lens[b];
+    const int n = seq_tiles(p, len);
+    if (n == 0) {
+      const int owner = min(pref / sc.T, sc.n_pairs - 1);
+      if (owner > sc.pair) return false;
+      ++cur.b;
+      if (owner < sc.pair) continue;
+      sg.b = b;
+      sg.t0 = sg.t1 = 0;
+      sg.kind = kSegZero;
+      return true;
+    }
+    if (pref >= sc.hi) return false;
+    ++cur.b;
+    cur.pref = pref + n;
+    const int g0 = max(pref, sc.lo), g1 = min(pref + n, sc.hi);
+    if (g1 <= g0) continue;
+    sg.b = b;
+    sg.t0 = (g0 - pref) * kT;
+    sg.t1 = min(len, (g1 - pref) * kT);
+    sg.kind = (g0 == pref && g1 == pref + n) ? kSegDirect : kSegPartial;
+    return true;
+  }
+  return false;
+}
+
 template <bool kBF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ CUtensorMap tm_qa,
-                       const __grid_constant__ CUtensorMap tm_c, const MlaParams p) {
+                       const __grid_constant__ CUtensorMap tm_c,
+                       const __grid_constant__ CUtensorMap tm_out,
+                       const __grid_constant__ CUtensorMap tm_po, const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -116,31 +178,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBars + kNumBars * 8 + 4);
 
   const uint32_t rank = cluster_ctarank();
-  const int split = blockIdx.x >> 1;
-  const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col0 = static_cast<int>(rank) * 256;  // this CTA's O columns
 
-  // ---------------- range and data checks (identical on both CTAs)
-  const int seq_len = p.seq_lens[b];
-  int bad = 0;
-  if (seq_len < 0 || seq_len > p.max_seq_len) {
-    bad = 1;
-    if (threadIdx.x == 0 && split == 0 && rank == 0) flag_error(p.err_flag, kFlagBadSeqLen);
-  }
-  const int t_begin = split * p.tokens_per_split;
-  const int t_end = bad ? t_begin : min(seq_len, t_begin + p.tokens_per_split);
-  if (!bad && t_end > t_begin) {
-    const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
-    const int k1 = (t_end - 1) >> p.log2_block_size;
-    for (int k = (t_begin >> p.log2_block_size) + threadIdx.x; k <= k1; k += blockDim.x) {
-      const int id = bt[k];
-      if (id < 0 || id >= p.num_blocks) {
-        bad = 1;
-        if (rank == 0) flag_error(p.err_flag, kFlagBadBlock);
-      }
+  // ---------------- schedule: block-wide scan of the per-sequence tile counts
+  Sched sc;
+  sc.pair = static_cast<int>(blockIdx.x >> 1);
+  sc.n_pairs = static_cast<int>(gridDim.x >> 1);
+  Cursor cur0;
+  {
+    int* s_warp = reinterpret_cast<int*>(smem + kOffRed);  // [0, 32) totals, [32, 64) scanned
+    int* s_misc = s_warp + 64;                              // b_start, its first tile
+    constexpr int kWarpsAll = kThreads / 32;
+    const int chunk = (p.batch + kThreads - 1) / kThreads;
+    const int b_a = min(p.batch, static_cast<int>(threadIdx.x) * chunk);
+    const int b_b = min(p.batch, b_a + chunk);
+    int sum = 0;
+    bool bad_len = false;
+    for (int b = b_a; b < b_b; ++b) {
+      const int len = p.seq_lens[b];
+      bad_len |= (len < 0 || len > p.max_seq_len);
+      sum += seq_tiles(p, len);
     }
+    if (bad_len && sc.pair == 0 && rank == 0) flag_error(p.err_flag, kFlagBadSeqLen);
+    int x = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    if (threadIdx.x == 0) s_misc[0] = p.batch;
+    __syncthreads();
+    if (warp == 0) {
+      int v = lane < kWarpsAll ? s_warp[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += y;
+      }
+      s_warp[32 + lane] = v;
+    }
+    __syncthreads();
+    const int t_all = s_warp[32 + kWarpsAll - 1];
+    sc.T = max(1, (t_all + sc.n_pairs - 1) / sc.n_pairs);
+    sc.lo = sc.pair * sc.T;
+    sc.hi = min(sc.lo + sc.T, t_all);
+    // First sequence this pair touches: pref_b + max(n_b, 1) > lo.
+    const int excl = (warp > 0 ? s_warp[32 + warp - 1] : 0) + x - sum;
+    int pref = excl, cand = p.batch, cand_pref = 0;
+    for (int b = b_a; b < b_b; ++b) {
+      const int n = seq_tiles(p, p.seq_lens[b]);
+      if (cand == p.batch && pref + max(n, 1) > sc.lo) {
+        cand = b;
+        cand_pref = pref;
+      }
+      if (p.ws_hdr && sc.pair == 0 && rank == 0) p.ws_hdr[kHdrPref + b] = pref;
+      pref += n;
+    }
+    if (cand < p.batch) atomicMin(&s_misc[0], cand);
+    if (p.ws_hdr && sc.pair == 0 && rank == 0 && threadIdx.x == 0) {
+      p.ws_hdr[0] = sc.T;
+      p.ws_hdr[1] = t_all;
+      p.ws_hdr[kHdrPref + p.batch] = t_all;
+    }
+    __syncthreads();
+    if (cand < p.batch && cand == s_misc[0]) s_misc[1] = cand_pref;
+    __syncthreads();
+    cur0.b = s_misc[0];
+    cur0.pref = cur0.b < p.batch ? s_misc[1] : 0;
   }
+
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), kSoftmaxThreads);
     mbar_init(bar(kBarQs), 1);
@@ -155,31 +263,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarSFree), kSoftmaxThreads);
     mbar_init(bar(kBarPFull), kSoftmaxThreads);
     mbar_init(bar(kBarPvDone), 1);
+    mbar_init(bar(kBarEpiW), kSoftmaxThreads);
+    mbar_init(bar(kBarEpiR), 1);
+    mbar_init(bar(kBarEpiDone), 1);
     mbar_init(bar(kBarDrain), 1);
     *abort_word = 0;
     fence_barrier_init();
   }
-  bad = __syncthreads_or(bad);
-  cluster_sync();
-
-  const size_t head0 = static_cast<size_t>(b) * kMlaHeads;
-  if (bad || t_end <= t_begin) {
-    for (int e = threadIdx.x; e < kMlaHeads * 256; e += blockDim.x) {
-      const int h = e >> 8, c = col0 + (e & 255);
-      if (p.n_split == 1) {
-        static_cast<uint16_t*>(p.out)[(head0 + h) * kMlaDc + c] = 0;
-      } else {
-        p.part_o[((head0 + h) * p.n_split + split) * kMlaDc + c] = 0.f;
-        if (rank == 0 && (e & 255) == 0)
-          p.part_lse[(head0 + h) * p.n_split + split] = bad ? DECATTN_POISON_LSE : kNegInf;
-      }
-    }
-    cluster_sync();
-    return;
-  }
-
-  const int n_tiles = (t_end - t_begin + kT - 1) / kT;
-
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -187,6 +277,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_sync();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 8) {
@@ -194,24 +285,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_c);
       tma_prefetch_desc(&tm_qa);
-      mbar_arrive_expect_tx(bar(kBarQs), kQSmemChunks * kQChunkBytes);
-      for (int c = 0; c < kQSmemChunks; ++c)
-        tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_qa, c * kChunk,
-                    static_cast<int>(head0), bar(kBarQs));
-      const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
       const int bs = p.block_size;
       const int rows_per_box = bs < kBoxRows ? bs : kBoxRows;
+      int g = 0;          // global tile index (ring stage and phase)
+      int s_issued = 0;   // tiles whose score part is requested
+      int v_issued = 0;   // tiles whose value part is requested
+      int q_issued = 0;   // segments whose Q part is requested
+      bool ok = true;
       // A stage holds all 9 column chunks of a tile.  This CTA's 4 value
       // chunks (latent columns [256 r, 256 r + 256)) stay until PV(j); the
       // other 5 are only read by S(j) and are refilled as soon as S(j) is
       // done, so loads run ahead of the PV that would otherwise gate them.
-      auto load_part = [&](int it, bool value_part) -> bool {
-        const int s = it % kStages;
+      auto load_part = [&](const int32_t* bt, int t_lo, int t_hi, int it, bool value_part) -> bool {
+        const int gi = g + it;
+        const int s = gi % kStages;
         const uint32_t empty = bar((value_part ? kBarKvEmptyV : kBarKvEmptyS) + s);
-        if (!mbar_wait_or_abort(empty, ((it / kStages) & 1) ^ 1, p.err_flag, abort_word))
+        if (!mbar_wait_or_abort(empty, ((gi / kStages) & 1) ^ 1, p.err_flag, abort_word))
           return false;
-        const int t0 = t_begin + it * kT;
-        const int nval = min(kT, t_end - t0);
+        const int t0 = t_lo + it * kT;
+        const int nval = min(kT, t_hi - t0);
         const int nbox = (nval + rows_per_box - 1) / rows_per_box;
         const uint32_t st = sbase + kOffRing + s * kStageBytes;
         const int nparts = value_part ? 4 : kChunks - 4;
@@ -219,6 +311,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                               static_cast<uint32_t>(nbox * nparts * rows_per_box * 128));
         for (int k = 0; k < nbox; ++k) {
           const int t = t0 + k * rows_per_box;
+          // A block id outside [0, num_blocks) lands the box outside the
+          // cache tensor, where the copy reads zeros; the softmax warps flag
+          // the segment and zero its result.
           const int row = bt[t >> p.log2_block_size] * bs + (t & (bs - 1));
           const uint32_t off = static_cast<uint32_t>(k * rows_per_box * 128);
           // Default L2 policy: the peer CTA loads the same tile moments later.
@@ -228,21 +323,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d(st + c * kCChunkBytes + off, &tm_c, c * kChunk, row, bar(kBarKvFull + s));
           }
         }
+        if (value_part) v_issued = gi + 1; else s_issued = gi + 1;
         return true;
       };
-      // The tensor pipe completes PV(j - 2) before S(j - 1), so the value
-      // part of tile j is requested before the score part of tile j + 1.
-      int issued = 0;
-      bool ok = load_part(0, false);
-      for (int it = 0; ok && it < n_tiles; ++it) {
-        ok = load_part(it, true);
-        if (ok) issued = it + 1;
-        if (ok && it + 1 < n_tiles) ok = load_part(it + 1, false);
-      }
-      for (int it = max(0, issued - kStages); it < issued; ++it)
-        if (!mbar_wait_or_abort(bar(kBarKvFull + it % kStages), (it / kStages) & 1, p.err_flag,
-                                abort_word))
+      Cursor cur = cur0;
+      Seg sg;
+      while (ok && next_seg(p, sc, cur, sg)) {
+        if (sg.kind == kSegZero) continue;
+        const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
+        // Q[:, 0:256) of this segment's sequence, once the previous
+        // segment's epilogue (which stages its output in the same shared
+        // memory, after that segment's last S) is done with it.
+        if (q_issued > 0 &&
+            !mbar_wait_or_abort(bar(kBarEpiDone), (q_issued - 1) & 1, p.err_flag, abort_word)) {
+          ok = false;
           break;
+        }
+        mbar_arrive_expect_tx(bar(kBarQs), kQSmemChunks * kQChunkBytes);
+        for (int c = 0; c < kQSmemChunks; ++c)
+          tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_qa, c * kChunk, sg.b * kMlaHeads,
+                      bar(kBarQs));
+        ++q_issued;
+        const int32_t* bt = p.block_table + static_cast<size_t>(sg.b) * p.max_blocks_per_seq;
+        // The tensor pipe completes PV(j - 2) before S(j - 1), so the value
+        // part of tile j is requested before the score part of tile j + 1.
+        ok = load_part(bt, sg.t0, sg.t1, 0, false);
+        for (int it = 0; ok && it < n; ++it) {
+          ok = load_part(bt, sg.t0, sg.t1, it, true);
+          if (ok && it + 1 < n) ok = load_part(bt, sg.t0, sg.t1, it + 1, false);
+        }
+        g += n;
+      }
+      // Wait for this thread's copies still in flight before the CTA may
+      // exit, even when another thread has raised the abort word: a bulk
+      // copy must never land in the shared memory of a finished CTA.  A tile
+      // whose value part was never requested gets the missing arrival so
+      // that its phase completes once the score part has landed.  Each wait
+      // is bounded on its own.
+      if (v_issued < s_issued) mbar_arrive(bar(kBarKvFull + (s_issued - 1) % kStages));
+      for (int it = max(0, s_issued - kStages); it < s_issued; ++it)
+        if (!mbar_wait(bar(kBarKvFull + it % kStages), (it / kStages) & 1, p.err_flag)) break;
+      if (q_issued > 0) mbar_wait(bar(kBarQs), (q_issued - 1) & 1, p.err_flag);
     }
   } else if (warp == 9) {
     // ---------------- MMA issuer (one thread)
@@ -271,6 +392,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint64_t db = dr + static_cast<uint64_t>(s) * kStageUnits;
         const uint32_t d = tmem + kTmemS;
+        // Fully unrolled: a rolled chunk loop measurably slows the issue of
+        // this 36-MMA chain (1.5 vs 1.2 us per tile on GB300).
 #pragma unroll
         for (int c = 0; c < kQSmemChunks; ++c) {
 #pragma unroll
@@ -289,27 +412,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_commit(bar(kBarKvEmptyS + s));
         return true;
       };
-      // O += P(j) C_lat(j) over this CTA's 256 value columns (MN-major B).
-      auto issue_pv = [&](int j) -> bool {
+      // O += P(j) C_lat(j) over this CTA's 256 value columns (MN-major B);
+      // the first tile of a segment overwrites O.
+      auto issue_pv = [&](int j, bool first) -> bool {
         if (!mbar_wait_or_abort(bar(kBarPFull), j & 1, p.err_flag, abort_word)) return false;
         tc_fence_after();
         const uint64_t db = dv + static_cast<uint64_t>(j % kStages) * kStageUnits;
 #pragma unroll
         for (int ks = 0; ks < kT / 16; ++ks)
           tc_mma_f16_ts(tmem + kTmemO, tmem + kTmemP + ks * 8, db + ks * (2048 >> 4), idesc_pv,
-                        (j > 0 || ks > 0) ? 1u : 0u);
+                        (!first || ks > 0) ? 1u : 0u);
         tc_commit(bar(kBarPvDone));
         tc_commit(bar(kBarKvEmptyV + j % kStages));
         return true;
       };
-      // PV(j) goes before S(j + 1): the value chunks of tile j are released
-      // (and the load of tile j + 2 starts) as early as possible.
-      bool ok = mbar_wait_or_abort(bar(kBarQ), 0, p.err_flag, abort_word) &&
-                mbar_wait_or_abort(bar(kBarQs), 0, p.err_flag, abort_word);
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        ok = issue_pv(j);
-        if (ok && j + 1 < n_tiles) ok = issue_s(j + 1);
+      // Per segment: wait for its Q (TMEM part written by the softmax warps
+      // after the previous segment's epilogue, so O is free again), then
+      // S(j), PV(j), S(j + 1), ...  PV(j) goes before S(j + 1): the value
+      // chunks of tile j are released (and the load of tile j + 2 starts) as
+      // early as possible.
+      bool ok = true;
+      int g = 0, k = 0;
+      Cursor cur = cur0;
+      Seg sg;
+      while (ok && next_seg(p, sc, cur, sg)) {
+        if (sg.kind == kSegZero) continue;
+        const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
+        ok = mbar_wait_or_abort(bar(kBarQ), k & 1, p.err_flag, abort_word) &&
+             mbar_wait_or_abort(bar(kBarQs), k & 1, p.err_flag, abort_word);
+        for (int j = -1; ok && j < n; ++j) {  // j = -1 issues S(0) only
+          if (j >= 0) ok = issue_pv(g + j, j == 0);
+          if (ok && j + 1 < n) ok = issue_s(g + j + 1);
+        }
+        g += n;
+        ++k;
       }
       // Wait (bounded) until every MMA this thread issued has completed.
       tc_commit(bar(kBarDrain));
@@ -323,180 +459,294 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float* red_max = reinterpret_cast<float*>(smem + kOffRed);       // [2 slots][2 halves][128]
     float* red_sum = red_max + 2 * 2 * kMlaHeads;                    // [2 halves][128]
     const float scale = p.scale_log2;
-    float m_used = kNegInf, l = 0.f;  // l: this half's partial row sum
-
-    // Q row h, columns [256, 512) and the RoPE part, into TMEM (columns
-    // [0, 256) arrive in shared memory by TMA); the two halves split the
-    // five 64-column chunks 3 + 2, all loads in flight before any store.
-    {
-      const uint4* qa = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_abs) +
-                                                       (head0 + h) * kMlaDc) + 32;
-      const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_rope) +
-                                                       (head0 + h) * kMlaDr);
-      const int c0 = ch == 0 ? 0 : 3, nc = ch == 0 ? 3 : 2;
-      uint4 w[24];
-#pragma unroll
-      for (int k = 0; k < 24; ++k) {
-        const int c = c0 + k / 8;
-        if (k < nc * 8) w[k] = c < 4 ? qa[c * 8 + k % 8] : qr[k % 8];
-      }
-#pragma unroll
-      for (int cc = 0; cc < 3; ++cc) {
-        if (cc < nc) {
-          float v[32];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            v[4 * k] = __uint_as_float(w[cc * 8 + k].x);
-            v[4 * k + 1] = __uint_as_float(w[cc * 8 + k].y);
-            v[4 * k + 2] = __uint_as_float(w[cc * 8 + k].z);
-            v[4 * k + 3] = __uint_as_float(w[cc * 8 + k].w);
-          }
-          tmem_st32(tmem + lane_base + kTmemQ + (c0 + cc) * 32, v);
-        }
-      }
-      tc_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(kBarQ));
-    }
-
     bool ok = true;
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int nval = min(kT, t_end - (t_begin + j * kT));
-      const int nv = nval - ch * 32;  // valid columns in this half (may be <= 0 or > 32)
-      if (!mbar_wait_or_abort(bar(kBarSFull), j & 1, p.err_flag, abort_word)) {
-        ok = false;
-        break;
+    int g = 0, k = 0, epi_round = 0;
+    Cursor cur = cur0;
+    Seg sg;
+    while (ok && next_seg(p, sc, cur, sg)) {
+      const size_t head0 = static_cast<size_t>(sg.b) * kMlaHeads;
+      uint16_t* out_row = static_cast<uint16_t*>(p.out) + (head0 + h) * kMlaDc + col0 + ch * 128;
+      if (sg.kind == kSegZero) {
+        // An empty (or invalid-length) sequence: zero output rows.
+        uint4* dst = reinterpret_cast<uint4*>(out_row);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+        continue;
       }
-      tc_fence_after();
-      float s[32];
-      tmem_ld32(tmem + lane_base + kTmemS + ch * 32, s);
-      tc_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(kBarSFree));  // the MMA thread may now compute S(j + 1)
-      // Tile max of the scaled scores over this half (masked columns ignored).
-      if (nv < 32) {
+      const int n_tiles = (sg.t1 - sg.t0 + kT - 1) / kT;
+      float m_used = kNegInf, l = 0.f;  // l: this half's partial row sum
+
+      // Q row h, columns [256, 512) and the RoPE part, into TMEM (columns
+      // [0, 256) arrive in shared memory by TMA); the two halves split the
+      // five 64-column chunks 3 + 2, all loads in flight before any store.
+      // No MMA is in flight here: the previous segment's epilogue waited for
+      // its last PV, and this segment's first S waits for kBarQ.
+      {
+        const uint4* qa = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_abs) +
+                                                         (head0 + h) * kMlaDc) + 32;
+        const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_rope) +
+                                                         (head0 + h) * kMlaDr);
+        const int c0 = ch == 0 ? 0 : 3, nc = ch == 0 ? 3 : 2;
+        uint4 w[24];
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (k >= nv) s[k] = scale >= 0.f ? kNegInf : -kNegInf;
-      }
-      float mx[16];
+        for (int kk = 0; kk < 24; ++kk) {
+          const int c = c0 + kk / 8;
+          if (kk < nc * 8) w[kk] = c < 4 ? qa[c * 8 + kk % 8] : qr[kk % 8];
+        }
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        mx[k] = scale >= 0.f ? fmaxf(s[k], s[k + 16]) : fminf(s[k], s[k + 16]);
+        for (int cc = 0; cc < 3; ++cc) {
+          if (cc < nc) {
+            float v[32];
 #pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-        for (int k = 0; k < w; ++k)
-          mx[k] = scale >= 0.f ? fmaxf(mx[k], mx[k + w]) : fminf(mx[k], mx[k + w]);
-      float mt = mx[0] * scale;
-      if (mt != mt) mt = kNegInf;  // an all-masked half (-inf * 0 cannot occur: scale != 0)
-      // Swap halves' maxima: slot j & 1 of the exchange area.
-      red_max[((j & 1) * 2 + ch) * kMlaHeads + h] = mt;
-      mbar_arrive(bar(kBarMax));
-      if (!mbar_wait_or_abort(bar(kBarMax), j & 1, p.err_flag, abort_word)) {
-        ok = false;
-        break;
-      }
-      mt = fmaxf(mt, red_max[((j & 1) * 2 + (ch ^ 1)) * kMlaHeads + h]);
-      // P(j - 1) must have been consumed (and O updated) before P(j) is
-      // written or O is rescaled.
-      if (j > 0 && !mbar_wait_or_abort(bar(kBarPvDone), (j - 1) & 1, p.err_flag, abort_word)) {
-        ok = false;
-        break;
-      }
-      const bool need = mt > m_used + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? mt : m_used;
-        const float factor = need ? ex2(m_used - m_new) : 1.f;  // 0 when m_used = -inf
-        if (j > 0) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = ch * 128; c < ch * 128 + 128; c += 32) {
-            float o[32];
-            tmem_ld32(tmem + lane_base + kTmemO + c, o);
-            tc_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] *= factor;
-            tmem_st32(tmem + lane_base + kTmemO + c, o);
+            for (int kk = 0; kk < 8; ++kk) {
+              v[4 * kk] = __uint_as_float(w[cc * 8 + kk].x);
+              v[4 * kk + 1] = __uint_as_float(w[cc * 8 + kk].y);
+              v[4 * kk + 2] = __uint_as_float(w[cc * 8 + kk].z);
+              v[4 * kk + 3] = __uint_as_float(w[cc * 8 + kk].w);
+            }
+            tmem_st32(tmem + lane_base + kTmemQ + (c0 + cc) * 32, v);
           }
         }
-        l *= factor;
-        m_used = m_new;
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarQ));
       }
-      // p = 2^(s scale - m_used) (one FFMA + EX2), partial row sum, P(j) half
-      // into TMEM (two 16-bit values per column).
-      const float neg_m = -m_used;
-      uint32_t pk[16];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        float p0 = ex2(fmaf(s[2 * k], scale, neg_m));
-        float p1 = ex2(fmaf(s[2 * k + 1], scale, neg_m));
-        if (nv < 32) {
-          p0 = 2 * k < nv ? p0 : 0.f;
-          p1 = 2 * k + 1 < nv ? p1 : 0.f;
+      // Block ids of the segment (needed by the epilogue only, so checked
+      // while the first tile is in flight): every warp checks all of them,
+      // so the verdict is uniform without a CTA-wide barrier.
+      bool seg_bad = false;
+      {
+        const int32_t* bt = p.block_table + static_cast<size_t>(sg.b) * p.max_blocks_per_seq;
+        const int k1 = (sg.t1 - 1) >> p.log2_block_size;
+        for (int kb = (sg.t0 >> p.log2_block_size) + lane; kb <= k1; kb += 32) {
+          const int id = bt[kb];
+          seg_bad |= (id < 0 || id >= p.num_blocks);
         }
-        ls[k & 3] += p0 + p1;
-        pk[k] = pack2<kBF16>(p0, p1);
+        seg_bad = __any_sync(0xffffffffu, seg_bad);
+        if (seg_bad && rank == 0 && threadIdx.x == 0) flag_error(p.err_flag, kFlagBadBlock);
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      tmem_st16(tmem + lane_base + kTmemP + ch * 16, pk);
-      if (nval < kT) {
-        // Value rows past the sequence end may hold anything (even NaN): zero
-        // them so that P = 0 there contributes exactly nothing.
-        uint8_t* st = smem + kOffRing + (j % kStages) * kStageBytes + rank * 4 * kCChunkBytes;
-        const int t = ch * 128 + h;
-        for (int e = t; e < (kT - nval) * 4 * 8; e += kSoftmaxThreads) {
-          const int row = nval + e / 32, c = (e / 8) & 3, q = e & 7;
-          *reinterpret_cast<uint4*>(st + c * kCChunkBytes + row * 128 + q * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
-      tc_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(kBarPFull));
-    }
 
-    // ---------------- epilogue: O row h, this thread's 128 columns, / l
-    if (ok) {
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int gj = g + j;
+        const int nval = min(kT, sg.t1 - (sg.t0 + j * kT));
+        const int nv = nval - ch * 32;  // valid columns in this half (may be <= 0 or > 32)
+        if (!mbar_wait_or_abort(bar(kBarSFull), gj & 1, p.err_flag, abort_word)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[32];
+        tmem_ld32(tmem + lane_base + kTmemS + ch * 32, s);
+        tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(kBarSFree));  // the MMA thread may now compute S(j + 1)
+        // Tile max of the scaled scores over this half (masked columns ignored).
+        if (nv < 32) {
+#pragma unroll
+          for (int kk = 0; kk < 32; ++kk)
+            if (kk >= nv) s[kk] = scale >= 0.f ? kNegInf : -kNegInf;
+        }
+        float mx[16];
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+          mx[kk] = scale >= 0.f ? fmaxf(s[kk], s[kk + 16]) : fminf(s[kk], s[kk + 16]);
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int kk = 0; kk < w; ++kk)
+            mx[kk] = scale >= 0.f ? fmaxf(mx[kk], mx[kk + w]) : fminf(mx[kk], mx[kk + w]);
+        float mt = mx[0] * scale;
+        if (mt != mt) mt = kNegInf;  // an all-masked half (-inf * 0 cannot occur: scale != 0)
+        // Post this half's maximum for the partner half (slot gj & 1) and
+        // go on without waiting: the exponentials below are computed against
+        // the current running max m_used, which stays valid unless a score of
+        // either half exceeds it by more than the rescale threshold -- rare
+        // after the first tile.  The exchange completes meanwhile.
+        red_max[((gj & 1) * 2 + ch) * kMlaHeads + h] = mt;
+        mbar_arrive(bar(kBarMax));
+        // P(j - 1) must have been consumed (and O updated) before P(j) is
+        // written or O is rescaled.  (The previous segment's last PV was
+        // waited for by its epilogue.)
+        if (j > 0 &&
+            !mbar_wait_or_abort(bar(kBarPvDone), (gj - 1) & 1, p.err_flag, abort_word)) {
+          ok = false;
+          break;
+        }
+        // p = 2^(s scale - m) (one FFMA + EX2), partial row sum, P packed two
+        // 16-bit values per TMEM column.
+        uint32_t pk[16];
+        auto exps = [&](float neg_m) -> float {
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            float p0 = ex2(fmaf(s[2 * kk], scale, neg_m));
+            float p1 = ex2(fmaf(s[2 * kk + 1], scale, neg_m));
+            if (nv < 32) {
+              p0 = 2 * kk < nv ? p0 : 0.f;
+              p1 = 2 * kk + 1 < nv ? p1 : 0.f;
+            }
+            ls[kk & 3] += p0 + p1;
+            pk[kk] = pack2<kBF16>(p0, p1);
+          }
+          return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        };
+        float lt_tile = 0.f;
+        if (m_used != kNegInf) lt_tile = exps(-m_used);
+        if (!mbar_wait_or_abort(bar(kBarMax), gj & 1, p.err_flag, abort_word)) {
+          ok = false;
+          break;
+        }
+        mt = fmaxf(mt, red_max[((gj & 1) * 2 + (ch ^ 1)) * kMlaHeads + h]);
+        const bool need = mt > m_used + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mt : m_used;
+          const float factor = need ? ex2(m_used - m_new) : 1.f;  // 0 when m_used = -inf
+          if (j > 0) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = ch * 128; c < ch * 128 + 128; c += 32) {
+              float o[32];
+              tmem_ld32(tmem + lane_base + kTmemO + c, o);
+              tc_wait_ld();
+#pragma unroll
+              for (int kk = 0; kk < 32; ++kk) o[kk] *= factor;
+              tmem_st32(tmem + lane_base + kTmemO + c, o);
+            }
+          }
+          l *= factor;
+          m_used = m_new;
+          lt_tile = exps(-m_used);  // the speculative values were against the old max
+        }
+        l += lt_tile;
+        tmem_st16(tmem + lane_base + kTmemP + ch * 16, pk);
+        if (nval < kT) {
+          // Value rows past the sequence end may hold anything (even NaN): zero
+          // them so that P = 0 there contributes exactly nothing.
+          uint8_t* st = smem + kOffRing + (gj % kStages) * kStageBytes + rank * 4 * kCChunkBytes;
+          const int t = ch * 128 + h;
+          for (int e = t; e < (kT - nval) * 4 * 8; e += kSoftmaxThreads) {
+            const int row = nval + e / 32, c = (e / 8) & 3, q = e & 7;
+            *reinterpret_cast<uint4*>(st + c * kCChunkBytes + row * 128 + q * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull));
+      }
+      if (!ok) break;
+
+      // Pull the next segment's Q row into L2 now; its TMEM load follows
+      // this epilogue on the critical path of the segment switch.
+      {
+        Cursor c2 = cur;
+        Seg nx;
+        bool have = false;
+        while (!have && next_seg(p, sc, c2, nx)) have = nx.kind != kSegZero;
+        if (have) {
+          const char* row = reinterpret_cast<const char*>(
+              static_cast<const uint16_t*>(p.q_abs) + (static_cast<size_t>(nx.b) * kMlaHeads + h) * kMlaDc);
+          if (ch == 0) {
+            prefetch_l2(row + 512);
+            prefetch_l2(row + 640);
+            prefetch_l2(row + 768);
+          } else {
+            prefetch_l2(row + 896);
+            prefetch_l2(static_cast<const uint16_t*>(p.q_rope) +
+                        (static_cast<size_t>(nx.b) * kMlaHeads + h) * kMlaDr);
+          }
+        }
+      }
+
+      // ---------------- epilogue: O row h, this thread's 128 columns, / l
       red_sum[ch * kMlaHeads + h] = l;
       mbar_arrive(bar(kBarSum));
-      ok = mbar_wait_or_abort(bar(kBarSum), 0, p.err_flag, abort_word) &&
-           mbar_wait_or_abort(bar(kBarPvDone), (n_tiles - 1) & 1, p.err_flag, abort_word);
-    }
-    if (ok) {
+      ok = mbar_wait_or_abort(bar(kBarSum), k & 1, p.err_flag, abort_word) &&
+           mbar_wait_or_abort(bar(kBarPvDone), (g + n_tiles - 1) & 1, p.err_flag, abort_word);
+      if (!ok) break;
       const float lt = l + red_sum[(ch ^ 1) * kMlaHeads + h];
       tc_fence_after();
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float inv = (lt > 0.f && !seg_bad) ? 1.f / lt : 0.f;
+      const bool partial = sg.kind == kSegPartial;
+      const int slot = 2 * sc.pair + (k == 0 ? 0 : 1);
+      if (partial && rank == 0 && ch == 0)
+        p.part_lse[static_cast<size_t>(slot) * kMlaHeads + h] =
+            seg_bad ? DECATTN_POISON_LSE : (lt > 0.f ? m_used + lg2(lt) : kNegInf);
+      // O / l leaves through shared memory and bulk tensor stores: the Q
+      // region (free: this segment's last S is done) holds four 128-row
+      // boxes of 128-byte rows, 128-byte swizzled (16-byte chunk j of row y
+      // at chunk j ^ (y % 8), conflict-free for a warp writing 32 rows).  An
+      // fp32 partial (this CTA's 256 columns = 8 boxes of 32) takes two
+      // rounds, a 16-bit output (4 boxes of 64 columns) one.
+      const int rounds = partial ? 2 : 1;
+      for (int r = 0; ok && r < rounds; ++r) {
 #pragma unroll 1
-      for (int c = ch * 128; c < ch * 128 + 128; c += 32) {
-        float o[32];
-        tmem_ld32(tmem + lane_base + kTmemO + c, o);
-        tc_wait_ld();
-        if (p.n_split == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                                (head0 + h) * kMlaDc + col0 + c);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int bi = ch * 2 + cc;
+          uint8_t* box = smem + kOffQ + bi * (kQChunkBytes);
+          uint4 v[8];
+          if (partial) {
+            float o[32];
+            tmem_ld32(tmem + lane_base + kTmemO + ch * 128 + r * 64 + cc * 32, o);
+            tc_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst[k] = make_uint4(pack2<kBF16>(o[8 * k] * inv, o[8 * k + 1] * inv),
-                                pack2<kBF16>(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
-                                pack2<kBF16>(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
-                                pack2<kBF16>(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(
-              p.part_o + ((head0 + h) * p.n_split + split) * kMlaDc + col0 + c);
+            for (int q = 0; q < 8; ++q)
+              v[q] = make_uint4(__float_as_uint(o[4 * q] * inv), __float_as_uint(o[4 * q + 1] * inv),
+                                __float_as_uint(o[4 * q + 2] * inv),
+                                __float_as_uint(o[4 * q + 3] * inv));
+          } else {
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(o[4 * k] * inv, o[4 * k + 1] * inv, o[4 * k + 2] * inv,
-                                 o[4 * k + 3] * inv);
+            for (int half = 0; half < 2; ++half) {
+              float o[32];
+              tmem_ld32(tmem + lane_base + kTmemO + ch * 128 + cc * 64 + half * 32, o);
+              tc_wait_ld();
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                v[half * 4 + q] = make_uint4(pack2<kBF16>(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                             pack2<kBF16>(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                             pack2<kBF16>(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                             pack2<kBF16>(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(box + h * 128 + ((q ^ (h & 7)) << 4)) = v[q];
         }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarEpiW));
+        if (threadIdx.x == 0) {
+          ok = mbar_wait_or_abort(bar(kBarEpiW), epi_round & 1, p.err_flag, abort_word);
+          if (ok) {
+            for (int bi = 0; bi < 4; ++bi) {
+              const uint32_t src = sbase + kOffQ + bi * kQChunkBytes;
+              if (partial)
+                tma_store_2d(&tm_po, col0 + (bi >> 1) * 128 + r * 64 + (bi & 1) * 32,
+                             slot * kMlaHeads, src);
+              else
+                tma_store_2d(&tm_out, col0 + (bi >> 1) * 128 + (bi & 1) * 64,
+                             static_cast<int>(head0), src);
+            }
+            bulk_commit_group();
+            bulk_wait_read_all();
+            mbar_arrive(bar(kBarEpiR));
+          }
+        }
+        if (ok) ok = mbar_wait_or_abort(bar(kBarEpiR), epi_round & 1, p.err_flag, abort_word);
+        ++epi_round;
       }
-      if (p.n_split > 1 && rank == 0 && ch == 0)
-        p.part_lse[(head0 + h) * p.n_split + split] = lt > 0.f ? m_used + lg2(lt) : kNegInf;
+      if (!ok) break;
+      if (threadIdx.x == 0) mbar_arrive(bar(kBarEpiDone));
+      // This thread's next segment writes Q into TMEM only now, after its
+      // own O reads; the MMA thread starts that segment (whose first PV
+      // overwrites O) only once all softmax threads have done so.
+      g += n_tiles;
+      ++k;
     }
   }
 
+  // The epilogue's bulk stores belong to thread 0: let them complete.
+  if (threadIdx.x == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 9) {
@@ -508,22 +758,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <bool kBF16>
 cudaError_t launch_t(const MlaParams& p, const CUtensorMap& tqa, const CUtensorMap& tc,
-                     cudaStream_t stream) {
+                     const CUtensorMap& tout, const CUtensorMap& tpo, cudaStream_t stream) {
   auto kern = mla_partial_kernel<kBF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(2 * p.n_split, p.batch);
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(tqa, tc, p);
+  dim3 grid(2 * p.n_pairs, 1);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(tqa, tc, tout, tpo, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_mla_partial(const MlaParams& p, const CUtensorMap& tm_qa,
-                               const CUtensorMap& tm_c, bool bf16, cudaStream_t stream) {
+                               const CUtensorMap& tm_c, const CUtensorMap& tm_out,
+                               const CUtensorMap& tm_po, bool bf16, cudaStream_t stream) {
   if (p.block_size > kT && (p.block_size % kT) != 0) return cudaErrorNotSupported;
-  return bf16 ? launch_t<true>(p, tm_qa, tm_c, stream) : launch_t<false>(p, tm_qa, tm_c, stream);
+  return bf16 ? launch_t<true>(p, tm_qa, tm_c, tm_out, tm_po, stream)
+              : launch_t<false>(p, tm_qa, tm_c, tm_out, tm_po, stream);
 }
 
 }  // namespace decattn

@@ -150,6 +150,11 @@ DECATTN_DEV void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Bring one global cache line into L2 (no register result, no completion).
+DECATTN_DEV void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)) : "memory");
+}
+
 // 2-D tiled bulk tensor load global -> shared, completion counted in bytes on bar.
 DECATTN_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
@@ -168,6 +173,27 @@ DECATTN_DEV void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
+
+// 2-D tiled bulk tensor store shared -> global, tracked by this thread's bulk
+// async-group (commit with bulk_commit_group, wait with bulk_wait_*).
+DECATTN_DEV void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+
+DECATTN_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until every committed bulk store of this thread has read its shared
+// memory source (the source may then be overwritten).
+DECATTN_DEV void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until every committed bulk store of this thread has completed.
+DECATTN_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 DECATTN_DEV uint64_t policy_evict_first() {
   uint64_t p;

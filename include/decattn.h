@@ -81,7 +81,9 @@ typedef enum { DECATTN_FP16 = 0, DECATTN_BF16 = 1 } decattn_dtype;
  *   max_blocks_per_seq row length of block_table
  *   max_seq_len        host upper bound on seq_lens[] (sizes the split grid;
  *                      must be <= max_blocks_per_seq * block_size)
- *   num_splits         split-KV chunks per sequence; 0 = automatic
+ *   num_splits         gqa_decode: split-KV chunks per sequence;
+ *                      mla_decode: CTA pairs sharing the batch's KV tiles
+ *                      (see mla_decode); 0 = automatic
  *   dtype              element type of every 16-bit tensor (decattn_dtype)
  *   workspace          device scratch of workspace_bytes bytes (may be NULL
  *                      when the required size is 0)
@@ -158,6 +160,14 @@ int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
  *                W_uv is applied by the caller)                      fp16/bf16
  *   scale        softmax scale (typically 1/sqrt(128 + 64))
  * s_t = scale * (q_absorbed . c_t + q_rope . k_rope_t).
+ *
+ * Work split: the 64-token tiles of all sequences, laid end to end, are cut
+ * into launch->num_splits equal shares (the planner's choice for 0), each
+ * streamed by one pair of CTAs; a share may cover the end of one sequence
+ * and the start of the next, so ragged batches stay balanced.  A sequence
+ * cut across shares is merged by a log-sum-exp combine; the workspace
+ * (mla_decode_workspace_size) holds a per-sequence tile table and two fp32
+ * partials per share.  num_splits = 1 needs no workspace.
  */
 int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_cache,
                const int32_t* block_table, const int32_t* seq_lens, void* out, float scale,
@@ -169,8 +179,9 @@ int gqa_decode_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq
                            int num_sms);
 int mla_decode_plan_splits(int batch, int max_seq_len, int num_sms);
 
-/* Workspace bytes needed for num_splits (>= 1) split-KV chunks: fp32 partial
- * outputs and log-sum-exps.  0 when num_splits == 1.  Returns 0 for invalid
+/* Workspace bytes needed for num_splits (>= 1): fp32 partial outputs and
+ * log-sum-exps (GQA: one per split per row; MLA: two per share, plus a
+ * per-sequence tile table).  0 when num_splits == 1.  Returns 0 for invalid
  * arguments as well; pure host arithmetic, no CUDA call. */
 size_t gqa_decode_workspace_size(int batch, int h_q, int d_head, int num_splits);
 size_t mla_decode_workspace_size(int batch, int num_splits);

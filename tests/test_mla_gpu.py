@@ -139,3 +139,45 @@ def test_output_is_deterministic():
     a = _run(x)
     b = _run(x)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# The balanced schedule lays all sequences' 64-token tiles end to end and
+# cuts them into num_splits equal shares, one per CTA pair.  These cases put
+# share boundaries at sequence starts, in the middle of sequences, next to
+# empty sequences, and leave pairs with nothing to do.
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 5, 9, 17, 64, 0])
+def test_balanced_shares_ragged_batch(num_splits):
+    lens = [0, 130, 64, 1, 700, 0, 257, 65, 3000, 63]
+    x = synth.mla_inputs(batch=len(lens), seq_lens=lens, block_size=16, seed=21, device=DEV)
+    _check(x, num_splits, n_rows=640, what=f"ragged shares={num_splits}")
+    out = _run(x, num_splits)
+    assert torch.all(out[0] == 0) and torch.all(out[5] == 0)
+
+
+@pytest.mark.parametrize("num_splits", [2, 3, 4, 6, 12])
+def test_share_boundaries_on_and_off_sequence_starts(num_splits):
+    # 6 sequences of 2 tiles: 3 / 6 / 12 shares start on sequence starts,
+    # 4 shares cut sequences in the middle.
+    x = synth.mla_inputs(batch=6, seq_lens=[128] * 6, block_size=64, seed=22, device=DEV)
+    _check(x, num_splits, n_rows=384, what=f"aligned shares={num_splits}")
+
+
+def test_more_pairs_than_tiles():
+    x = synth.mla_inputs(batch=2, seq_lens=[10, 70], block_size=32, seed=23, device=DEV)
+    _check(x, 8, what="8 pairs for 3 tiles")
+
+
+def test_bad_seq_len_between_cut_sequences():
+    x = synth.mla_inputs(batch=4, seq_lens=[500, 400, 300, 200], block_size=64, seed=24,
+                         device=DEV)
+    sl = x.seq_lens.clone()
+    sl[1] = x.max_seq_len + 1
+    xb = synth.MLAInputs(**{**x.__dict__, "seq_lens": sl})
+    for ns in (3, 7):
+        flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out = _run(xb, ns, err_flag=flag)
+        assert int(flag.item()) & da.FLAG_BAD_SEQ_LEN
+        assert torch.all(out[1] == 0)
+        rows = np.array([[b, i] for b in (0, 2, 3) for i in range(0, 128, 3)], np.int32)
+        ref, _ = oracle_mla(x, rows)
+        compare(gather_rows(out, rows), ref, f"rows around a bad length, shares={ns}")
