@@ -139,6 +139,63 @@ def gqa_inputs(batch: int, h_q: int, h_kv: int, d_head: int = 128, seq_lens=256,
                      scale=(1.0 / math.sqrt(d_head)) if scale is None else scale)
 
 
+@dataclass
+class GQAFp8Inputs:
+    q: torch.Tensor            # [B, h_q, d] fp16 / bf16
+    k_codes: torch.Tensor      # uint8 e4m3 codes [num_blocks, block_size, h_kv, d]
+    v_codes: torch.Tensor      # uint8 e4m3 codes [num_blocks, block_size, h_kv, d]
+    k_scale: torch.Tensor      # float32 [h_kv]: K value = e4m3(code) * k_scale[kv head]
+    v_scale: torch.Tensor      # float32 [h_kv]
+    block_table: torch.Tensor  # int32 [B, max_blocks_per_seq]
+    seq_lens: torch.Tensor     # int32 [B]
+    h_q: int
+    h_kv: int
+    d_head: int
+    block_size: int
+    num_blocks: int
+    max_seq_len: int
+    dtype: str                 # of q and out
+    scale: float
+
+    @property
+    def batch(self) -> int:
+        return self.q.shape[0]
+
+
+def gqa_fp8_inputs(batch: int, h_q: int, h_kv: int, d_head: int = 128, seq_lens=256,
+                   block_size: int = 16, dtype: str = "bf16", seed: int = 0,
+                   table: str = "permuted", q_std: float = 1.0, device="cpu",
+                   tail: str = "random", spare_blocks: int = 0,
+                   max_blocks_per_seq: int | None = None, scale: float | None = None,
+                   code_std: float = 112.0) -> GQAFp8Inputs:
+    """An 8-bit KV cache drawn directly in its storage format: codes are
+    N(0, code_std^2) samples rounded to e4m3 by torch (code_std = 112 puts
+    four standard deviations at the largest finite value, 448), and every KV
+    head gets its own K and V scale drawn uniformly from [0.5, 1.5] / code_std,
+    so the cached values are about unit-variance."""
+    sl = draw_seq_lens(batch, seq_lens, seed)
+    bt, nb = make_block_table(sl, block_size, table, seed, max_blocks_per_seq, spare_blocks)
+    g = _gen(device, seed)
+    q = _randn((batch, h_q, d_head), dtype, q_std, g, device)
+    shape = (nb, block_size, h_kv, d_head)
+    k = (torch.randn(shape, generator=g, device=device) * code_std).to(torch.float8_e4m3fn)
+    v = (torch.randn(shape, generator=g, device=device) * code_std).to(torch.float8_e4m3fn)
+    k, v = k.view(torch.uint8), v.view(torch.uint8)
+    ks = (torch.rand((h_kv,), generator=g, device=device) + 0.5) / code_std
+    vs = (torch.rand((h_kv,), generator=g, device=device) + 0.5) / code_std
+    if tail == "nan":
+        _fill_tails(k, bt, sl, block_size, 0x7F)  # the e4m3 NaN code
+        _fill_tails(v, bt, sl, block_size, 0x7F)
+    elif tail == "zero":
+        _fill_tails(k, bt, sl, block_size, 0)
+        _fill_tails(v, bt, sl, block_size, 0)
+    return GQAFp8Inputs(q=q, k_codes=k, v_codes=v, k_scale=ks.float(), v_scale=vs.float(),
+                        block_table=bt.to(device), seq_lens=sl.to(device), h_q=h_q, h_kv=h_kv,
+                        d_head=d_head, block_size=block_size, num_blocks=nb,
+                        max_seq_len=int(sl.max()) if batch else 0, dtype=dtype,
+                        scale=(1.0 / math.sqrt(d_head)) if scale is None else scale)
+
+
 MLA_HEADS = 128
 MLA_D_C = 512
 MLA_D_R = 64
@@ -203,6 +260,10 @@ WORKLOADS = {
     # Llama-3-70B-shaped layer, large batch: 64 query heads on 8 KV heads
     "llama3_70b_b64_s8k": ("gqa", dict(batch=64, h_q=64, h_kv=8, seq_lens=8192, block_size=16,
                                        dtype="bf16", table="permuted", q_std=0.5)),
+    # the same 70B-shaped layer over an 8-bit (e4m3) KV cache with per-KV-head scales
+    "llama3_70b_b64_s8k_fp8": ("gqa_fp8", dict(batch=64, h_q=64, h_kv=8, seq_lens=8192,
+                                               block_size=16, dtype="bf16", table="permuted",
+                                               q_std=0.5)),
     # DeepSeek-V2-shaped absorbed MLA layer
     "deepseek_v2_mla_b32_s8k": ("mla", dict(batch=32, seq_lens=8192, block_size=64,
                                             dtype="bf16", table="permuted")),
@@ -219,4 +280,6 @@ def workload_inputs(name: str, device="cpu", seed: int = 0, **overrides):
     kw = {**kw, **overrides}
     if kind == "gqa":
         return gqa_inputs(seed=seed, device=device, **kw)
+    if kind == "gqa_fp8":
+        return gqa_fp8_inputs(seed=seed, device=device, **kw)
     return mla_inputs(seed=seed, device=device, **kw)

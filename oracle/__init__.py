@@ -57,6 +57,9 @@ def _load():
             lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_to_double.restype = D
             lib.oracle_decode_array.argtypes = [P, I, I64, P]
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_double.restype = D
+            lib.oracle_dequant_e4m3.argtypes = [P, I64, I, I, P, P]
             lib.oracle_decode_array.restype = None
             lib.oracle_cache_row.argtypes = [P, I, I, I, I, I]
             lib.oracle_cache_row.restype = I64
@@ -111,6 +114,39 @@ def bf16_to_double(bits: np.ndarray) -> np.ndarray:
     dst = np.empty(src.shape, dtype=np.float64)
     _load().oracle_decode_array(_ptr(src), 1, src.size, _ptr(dst))
     return dst
+
+
+def e4m3_to_double(codes: np.ndarray) -> np.ndarray:
+    """Decode raw e4m3 codes (uint8) to float64."""
+    src = np.ascontiguousarray(codes, dtype=np.uint8)
+    lib = _load()
+    return np.array([lib.oracle_e4m3_to_double(int(c)) for c in src.reshape(-1)],
+                    dtype=np.float64).reshape(src.shape)
+
+
+def dequant_e4m3(codes: np.ndarray, scales) -> np.ndarray:
+    """Dequantise an e4m3 cache [..., h_kv, d] with one scale per KV head."""
+    src = np.ascontiguousarray(codes, dtype=np.uint8)
+    sc = np.ascontiguousarray(np.asarray(scales, dtype=np.float64).reshape(-1))
+    h_kv, d = src.shape[-2], src.shape[-1]
+    assert sc.shape == (h_kv,)
+    out = np.empty(src.shape, dtype=np.float64)
+    _load().oracle_dequant_e4m3(_ptr(src), src.size // (h_kv * d), h_kv, d, _ptr(sc), _ptr(out))
+    return out
+
+
+def gqa_decode_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens, *,
+                     q_dtype: str, scale: float, rows=None, t_begin: int = 0, t_end: int = -1):
+    """GQA decode over an e4m3 KV cache in fp64: dequantise K and V with their
+    per-KV-head scales, then the plain GQA definition (gqa_decode).
+
+    q [B, h_q, d] fp16/bf16 bits; k_codes, v_codes [num_blocks, block_size,
+    h_kv, d] uint8; k_scale, v_scale [h_kv].
+    """
+    q64 = half_to_double(q) if q_dtype == "fp16" else bf16_to_double(q)
+    return gqa_decode(q64, dequant_e4m3(k_codes, k_scale), dequant_e4m3(v_codes, v_scale),
+                      block_table, seq_lens, dtype="f64", scale=scale, rows=rows,
+                      t_begin=t_begin, t_end=t_end)
 
 
 def cache_row(block_table: np.ndarray, block_size: int, num_blocks: int, b: int, t: int) -> int:

@@ -34,8 +34,16 @@
  *     Reduce TPOT", "KV Cache Size by Attention Variant"; "MQA, GQA, and
  *     MLA", section 5 "CACHE SIZE COMPARISON").
  *
+ *   - 8-bit KV cache: e4m3 codes dequantised with one scale per KV head,
+ *     then the GQA decode above on the dequantised values ("Why GQA's KV
+ *     Cache Savings Don't Fully Reduce TPOT", "When the Serving Engineer
+ *     Doesn't Get to Choose the Model Architecture": an fp8 cache halves the
+ *     bytes and GQA quantises at KV-head granularity; "07 · MHA/MQA/GQA/MLA
+ *     quick learn", the question on changing the KV head count by a flag).
+ *
  * Element storage: dtype 0 = IEEE binary16, 1 = bfloat16, 2 = binary64.
- * The two 16-bit formats are decoded here from their bit-layout definitions.
+ * The two 16-bit formats and the 8-bit e4m3 format are decoded here from
+ * their bit-layout definitions.
  */
 #include <math.h>
 #include <stdint.h>
@@ -72,6 +80,38 @@ double oracle_bf16_to_double(uint16_t h) {
   float f;
   memcpy(&f, &w, sizeof f);
   return (double)f;
+}
+
+/* 8-bit float e4m3 (finite-only variant): 1 sign bit, 4 exponent bits
+ * (bias 7), 3 fraction bits.  Exponent field 0 holds subnormals
+ * frac * 2^-9; exponent field 15 with fraction 7 is NaN (the only
+ * non-finite code); every other code is (1 + frac/8) * 2^(e - 7).  Largest
+ * finite magnitude 448. */
+double oracle_e4m3_to_double(uint8_t c) {
+  int sign = (c >> 7) & 1;
+  int expo = (c >> 3) & 0xf;
+  int frac = c & 0x7;
+  double v;
+  if (expo == 0xf && frac == 0x7) {
+    v = NAN;
+  } else if (expo == 0) {
+    v = ldexp((double)frac, -9);
+  } else {
+    v = ldexp((double)(8 + frac), expo - 10); /* (1 + frac/8) * 2^(e-7) */
+  }
+  return sign ? -v : v;
+}
+
+/* Dequantise an e4m3 KV cache laid out [rows][h_kv][d] with one scale per KV
+ * head: out[r][j][e] = e4m3(codes[r][j][e]) * scale[j]. */
+void oracle_dequant_e4m3(const uint8_t* codes, int64_t rows, int h_kv, int d,
+                         const double* scale, double* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int j = 0; j < h_kv; ++j)
+      for (int e = 0; e < d; ++e) {
+        const int64_t i = (r * h_kv + j) * d + e;
+        out[i] = oracle_e4m3_to_double(codes[i]) * scale[j];
+      }
 }
 
 void oracle_decode_array(const uint16_t* src, int dtype, int64_t n, double* dst) {

@@ -384,3 +384,86 @@ def test_mla_latent_part_closed_form():
     p0 = math.exp(2.0) / (math.exp(2.0) + 1.0)
     expect = np.zeros(d_c); expect[3] = 2.0 * p0; expect[0] = 5.0 * p0
     np.testing.assert_allclose(out[0], expect, atol=1e-14)
+
+
+# ---------------------------------------------------------------- 8-bit (e4m3) KV cache
+
+def test_e4m3_decoding_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_to_double(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2  # 0x7f, 0xff
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_e4m3_closed_form_codes():
+    # sign | 4-bit exponent (bias 7) | 3-bit fraction; exponent 0 is subnormal.
+    cases = {0x00: 0.0, 0x01: 2.0**-9, 0x07: 7 * 2.0**-9, 0x08: 2.0**-6, 0x38: 1.0,
+             0x39: 1.125, 0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    got = oracle.e4m3_to_double(np.array(list(cases), np.uint8))
+    assert list(got) == list(cases.values())
+    assert math.copysign(1.0, oracle.e4m3_to_double(np.array([0x80], np.uint8))[0]) == -1.0
+    # monotone over the positive finite codes
+    pos = oracle.e4m3_to_double(np.arange(0x7F, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)
+
+
+def test_dequant_uses_the_scale_of_each_kv_head():
+    rows, h_kv, d = 3, 4, 5
+    codes = np.full((rows, h_kv, d), 0x38, np.uint8)  # every code is 1.0
+    scales = np.array([0.5, 2.0, 3.0, -1.25])
+    out = oracle.dequant_e4m3(codes, scales)
+    for j in range(h_kv):
+        assert np.all(out[:, j, :] == scales[j])
+
+
+def _fp8_case(rng, B=2, h_q=8, h_kv=2, d=16, S=(23, 9), bs=4):
+    nblk = [math.ceil(s / bs) for s in S]
+    table = np.full((B, max(nblk)), -1, np.int32)
+    perm = rng.permutation(sum(nblk) + 2).astype(np.int32)
+    k = 0
+    for b in range(B):
+        table[b, :nblk[b]] = perm[k:k + nblk[b]]
+        k += nblk[b]
+    nb = int(perm.max()) + 1
+    # finite e4m3 codes of moderate magnitude (|value| <= 8)
+    mags = np.array([c for c in range(0x60) if c != 0x7F], np.uint8)
+    kc = rng.choice(mags, size=(nb, bs, h_kv, d)) | (rng.integers(0, 2, (nb, bs, h_kv, d)) << 7).astype(np.uint8)
+    vc = rng.choice(mags, size=(nb, bs, h_kv, d)) | (rng.integers(0, 2, (nb, bs, h_kv, d)) << 7).astype(np.uint8)
+    q = torch.from_numpy(rng.standard_normal((B, h_q, d))).to(torch.bfloat16)
+    qbits = q.view(torch.int16).numpy().view(np.uint16)
+    return qbits, kc.astype(np.uint8), vc.astype(np.uint8), table, np.array(S, np.int32)
+
+
+def test_fp8kv_with_unit_scales_equals_the_16bit_path():
+    # Every e4m3 value is exactly representable in bfloat16, so the same cache
+    # stored as bf16 bits must give exactly the same fp64 result.
+    rng = np.random.default_rng(11)
+    q, kc, vc, bt, sl = _fp8_case(rng)
+    to_bf16 = lambda c: torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    ones = np.ones(kc.shape[2])
+    o1, l1 = oracle.gqa_decode_fp8kv(q, kc, vc, ones, ones, bt, sl, q_dtype="bf16", scale=0.2)
+    o2, l2 = oracle.gqa_decode(q, to_bf16(kc), to_bf16(vc), bt, sl, dtype="bf16", scale=0.2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_fp8kv_scales_act_on_scores_and_values_per_kv_head():
+    # V's scale multiplies the output of the heads that read that KV head; K's
+    # scale is the same as scaling those heads' queries.
+    rng = np.random.default_rng(12)
+    q, kc, vc, bt, sl = _fp8_case(rng, h_q=8, h_kv=2)
+    ks = np.array([0.75, 1.5])
+    vs = np.array([0.25, 4.0])
+    ones = np.ones(2)
+    o, lse = oracle.gqa_decode_fp8kv(q, kc, vc, ks, vs, bt, sl, q_dtype="bf16", scale=0.2)
+    q64 = oracle.bf16_to_double(q)
+    G = q.shape[1] // 2
+    qs = q64 * np.repeat(ks, G)[None, :, None]
+    o_ref, lse_ref = oracle.gqa_decode(qs, oracle.dequant_e4m3(kc, ones), oracle.dequant_e4m3(vc, ones),
+                                       bt, sl, dtype="f64", scale=0.2)
+    heads = np.tile(np.arange(q.shape[1]), q.shape[0])
+    np.testing.assert_allclose(o, o_ref * vs[heads // G][:, None], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-13, atol=1e-13)
