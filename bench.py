@@ -40,6 +40,7 @@ import torch  # noqa: E402
 METRIC = "decode-attn KV-read GB/s (% of GB300 HBM peak) and decode steps/s per layer"
 GQA_WORKLOAD = "llama3_70b_b64_s8k"
 MLA_WORKLOAD = "deepseek_v2_mla_b32_s8k"
+GQA_FP8_WORKLOAD = "llama3_70b_b64_s8k_fp8"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GQA_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/gqa_decode.cu", "gqa_mqa_mla_gb300/csrc/ptx.cuh",
                       "gqa_mqa_mla_gb300/csrc/internal.h"]
@@ -53,6 +54,11 @@ def gqa_bytes(x) -> int:
     e = 2
     kv = int(x.seq_lens.sum().item()) * x.h_kv * x.d_head * 2 * e
     return kv + 2 * x.batch * x.h_q * x.d_head * e
+
+
+def gqa_fp8_bytes(x) -> int:
+    kv = int(x.seq_lens.sum().item()) * x.h_kv * x.d_head * 2  # one byte per cached element
+    return kv + 2 * x.batch * x.h_q * x.d_head * 2 + 2 * x.h_kv * 4
 
 
 def mla_bytes(x) -> int:
@@ -276,6 +282,8 @@ def main():
     ap.add_argument("--parts", default="gqa,mla", help="comma list of gqa, mla")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the separately timed 8-bit-cache GQA layer (not part of value)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target wall time of the oracle CPU-baseline sample")
     ap.add_argument("--gqa-batch", type=int, default=None,
@@ -426,6 +434,45 @@ def main():
 
     peaks, peak_src = load_peaks()
     hbm = peaks["hbm_gbs"]
+
+    # ---------------- extra, outside the headline: the same 70B-shaped layer
+    # over an 8-bit e4m3 KV cache (half the cache bytes), timed on its own.
+    extras = None
+    if gx is not None and not args.no_extras:
+        fx = synth.workload_inputs(GQA_FP8_WORKLOAD, device=dev, seed=rank,
+                                   **({"batch": args.gqa_batch} if args.gqa_batch else {}))
+        f_ns = da.gqa_fp8_plan_splits(fx.batch, fx.h_q, fx.h_kv, fx.max_seq_len)
+        f_ws = torch.empty(max(16, da.gqa_workspace_size(fx.batch, fx.h_q, f_ns)),
+                           dtype=torch.uint8, device=dev)
+        f_out = torch.empty_like(fx.q)
+
+        def f_call():
+            da.gqa_decode_fp8kv(fx.q, fx.k_codes, fx.v_codes, fx.k_scale, fx.v_scale,
+                                fx.block_table, fx.seq_lens, scale=fx.scale,
+                                max_seq_len=fx.max_seq_len, out=f_out, num_splits=f_ns,
+                                workspace=f_ws, err_flag=flag)
+
+        for _ in range(5):
+            f_call()
+        torch.cuda.synchronize(dev)
+        nf = max(3, min(K, 500))
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(nf):
+            f_call()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        f_ms = f0.elapsed_time(f1) / nf
+        fb = gqa_fp8_bytes(fx)
+        f_gbps = fb / (f_ms * 1e-3) / 1e9
+        extras = {"gqa_fp8": {"workload": GQA_FP8_WORKLOAD, "GBps": f_gbps, "ms": f_ms,
+                              "steps_per_s": 1e3 / f_ms, "bytes": fb, "steps": nf,
+                              "frac_of_hbm_peak": f_gbps / hbm, "splits": f_ns,
+                              "cache_dtype": "e4m3 (per-KV-head fp32 scales)"}}
+        err |= int(flag.item())
+        del fx, f_ws, f_out
+
     parts_out = {}
     for name, ms in part_ms.items():
         gbps = part_bytes[name] / (ms * 1e-3) / 1e9
@@ -506,6 +553,7 @@ def main():
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "extras": extras,
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
         "err_flag": err,

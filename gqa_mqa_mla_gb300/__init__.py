@@ -1,6 +1,7 @@
 """libdecattn: GB300-native single-token decode attention over a paged KV cache.
 
-MHA / GQA / MQA (``gqa_decode``) and absorbed MLA (``mla_decode``), hand-written
+MHA / GQA / MQA (``gqa_decode``, and ``gqa_decode_fp8kv`` over an 8-bit e4m3 KV
+cache) and absorbed MLA (``mla_decode``), hand-written
 CUDA kernels for sm_103a behind a C ABI (include/decattn.h).  This package is
 the thin Python binding; ``synth`` draws seeded synthetic inputs.
 """
@@ -10,6 +11,8 @@ from .binding import (  # noqa: F401
     FLAG_BAD_SEQ_LEN,
     FLAG_TIMEOUT,
     gqa_decode,
+    gqa_decode_fp8kv,
+    gqa_fp8_plan_splits,
     gqa_plan_splits,
     gqa_workspace_size,
     kv_bytes_per_token,

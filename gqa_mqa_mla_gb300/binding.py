@@ -77,10 +77,14 @@ def lib() -> ctypes.CDLL:
             LP = ctypes.POINTER(Launch)
             L.gqa_decode.argtypes = [P, P, P, P, P, P, I, I, I, F, LP]
             L.gqa_decode.restype = I
+            L.gqa_decode_fp8kv.argtypes = [P, P, P, P, P, P, P, P, I, I, I, F, LP]
+            L.gqa_decode_fp8kv.restype = I
             L.mla_decode.argtypes = [P, P, P, P, P, P, F, LP]
             L.mla_decode.restype = I
             L.gqa_decode_plan_splits.argtypes = [I, I, I, I, I, I]
             L.gqa_decode_plan_splits.restype = I
+            L.gqa_decode_fp8kv_plan_splits.argtypes = [I, I, I, I, I, I]
+            L.gqa_decode_fp8kv_plan_splits.restype = I
             L.mla_decode_plan_splits.argtypes = [I, I, I]
             L.mla_decode_plan_splits.restype = I
             L.gqa_decode_workspace_size.argtypes = [I, I, I, I]
@@ -116,6 +120,14 @@ def gqa_plan_splits(batch: int, h_q: int, h_kv: int, max_seq_len: int, d_head: i
     r = lib().gqa_decode_plan_splits(batch, h_q, h_kv, d_head, max_seq_len, num_sms)
     if r < 0:
         raise DecAttnError("gqa_decode_plan_splits", r)
+    return r
+
+
+def gqa_fp8_plan_splits(batch: int, h_q: int, h_kv: int, max_seq_len: int, d_head: int = 128,
+                        num_sms: int = 0) -> int:
+    r = lib().gqa_decode_fp8kv_plan_splits(batch, h_q, h_kv, d_head, max_seq_len, num_sms)
+    if r < 0:
+        raise DecAttnError("gqa_decode_fp8kv_plan_splits", r)
     return r
 
 
@@ -197,6 +209,54 @@ def gqa_decode(q, k_cache, v_cache, block_table, seq_lens, *, scale: float, max_
                           d, float(scale), ctypes.byref(L))
     if st != DECATTN_OK:
         raise DecAttnError("gqa_decode", st)
+    return out
+
+
+def gqa_decode_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens, *,
+                     scale: float, max_seq_len: int, out=None, num_splits: int = 0,
+                     workspace=None, err_flag=None, stream=None):
+    """GQA decode over an 8-bit (e4m3) KV cache through the C ABI; returns out.
+
+    q [B, h_q, d] fp16/bf16; k_codes/v_codes uint8 (or float8_e4m3fn)
+    [num_blocks, block_size, h_kv, d]; k_scale/v_scale float32 [h_kv] (the
+    value of KV head j is e4m3(code) * scale[j]); the rest as gqa_decode.
+    """
+    _check(q, "q", ndim=3)
+    if q.dtype not in _DT:
+        raise TypeError("q must be float16 or bfloat16")
+    if k_codes.dtype == torch.float8_e4m3fn:
+        k_codes = k_codes.view(torch.uint8)
+    if v_codes.dtype == torch.float8_e4m3fn:
+        v_codes = v_codes.view(torch.uint8)
+    _check(k_codes, "k_codes", torch.uint8, 4)
+    _check(v_codes, "v_codes", torch.uint8, 4)
+    _check(k_scale, "k_scale", torch.float32, 1)
+    _check(v_scale, "v_scale", torch.float32, 1)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    B, h_q, d = q.shape
+    nb, bs, h_kv, d2 = k_codes.shape
+    if d2 != d or v_codes.shape != k_codes.shape:
+        raise ValueError("k_codes / v_codes shape mismatch")
+    if k_scale.shape != (h_kv,) or v_scale.shape != (h_kv,):
+        raise ValueError("k_scale / v_scale must be [h_kv]")
+    if h_kv < 1 or h_q % h_kv != 0:
+        raise ValueError(f"h_q={h_q} is not a multiple of h_kv={h_kv}")
+    if out is None:
+        out = torch.empty_like(q)
+    ns = num_splits if num_splits else gqa_fp8_plan_splits(B, h_q, h_kv, max_seq_len, d)
+    need = gqa_workspace_size(B, h_q, ns, d)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    L = make_launch(B, nb, bs, block_table.shape[1], max_seq_len, ns, _DT[q.dtype],
+                    _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                    _ptr(err_flag), _stream_handle(stream))
+    st = lib().gqa_decode_fp8kv(q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
+                                k_scale.data_ptr(), v_scale.data_ptr(), block_table.data_ptr(),
+                                seq_lens.data_ptr(), out.data_ptr(), h_q, h_kv, d, float(scale),
+                                ctypes.byref(L))
+    if st != DECATTN_OK:
+        raise DecAttnError("gqa_decode_fp8kv", st)
     return out
 
 

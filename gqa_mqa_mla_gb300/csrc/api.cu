@@ -112,6 +112,15 @@ int plan_gqa_splits(int batch, int /*h_q*/, int h_kv, int max_seq_len, int num_s
   return plan_splits(batch * h_kv, max_seq_len, num_sms * 2);
 }
 
+int plan_gqa_fp8_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms) {
+  // The 8-bit-cache kernel for 2..16 query heads per KV head runs three CTAs
+  // per SM (measured on the 70B-shaped layer: 2 splits 211 us, 1 split 233
+  // us); the other consumers, two.
+  const int group = h_kv > 0 ? h_q / h_kv : 1;
+  const int per_sm = (group >= 2 && group <= 16) ? 3 : 2;
+  return plan_splits(batch * h_kv, max_seq_len, num_sms * per_sm);
+}
+
 int plan_mla_splits(int batch, int max_seq_len, int num_sms) {
   // MLA partial kernel: one CTA pair per two SMs, all pairs resident at
   // once, each streaming an equal share of the batch's 64-token tiles.  Use
@@ -189,6 +198,15 @@ int gqa_decode_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq
   return plan_gqa_splits(batch, h_q, h_kv, max_seq_len, num_sms);
 }
 
+int gqa_decode_fp8kv_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,
+                                 int num_sms) {
+  if (batch < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 || d_head < 1 || max_seq_len < 0)
+    return DECATTN_ERR_INVALID_ARG;
+  if (num_sms <= 0) num_sms = device_sm_count();
+  if (num_sms <= 0) return DECATTN_ERR_CUDA;
+  return plan_gqa_fp8_splits(batch, h_q, h_kv, max_seq_len, num_sms);
+}
+
 int mla_decode_plan_splits(int batch, int max_seq_len, int num_sms) {
   if (batch < 1 || max_seq_len < 0) return DECATTN_ERR_INVALID_ARG;
   if (num_sms <= 0) num_sms = device_sm_count();
@@ -214,15 +232,20 @@ static int check_launch(const decattn_launch* L, bool mla) {
   return DECATTN_OK;
 }
 
-int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
-               const int32_t* block_table, const int32_t* seq_lens, void* out, int h_q, int h_kv,
-               int d_head, float scale, const decattn_launch* L) {
+// gqa_decode and gqa_decode_fp8kv share everything but the cache element type
+// (and the 8-bit cache's per-KV-head scales).
+static int gqa_decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                           const float* k_scale, const float* v_scale, bool fp8,
+                           const int32_t* block_table, const int32_t* seq_lens, void* out,
+                           int h_q, int h_kv, int d_head, float scale, const decattn_launch* L) {
   int st = check_launch(L, false);
   if (st != DECATTN_OK) return st;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
     return DECATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return DECATTN_ERR_INVALID_ARG;
+  if (fp8 && (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4)))
     return DECATTN_ERR_INVALID_ARG;
   if (h_q < 1 || h_kv < 1 || h_q % h_kv != 0) return DECATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return DECATTN_ERR_INVALID_ARG;
@@ -233,7 +256,8 @@ int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
   if (n_split == 0) {
     const int sms = device_sm_count();
     if (sms <= 0) return DECATTN_ERR_CUDA;
-    n_split = plan_gqa_splits(L->batch, h_q, h_kv, L->max_seq_len, sms);
+    n_split = fp8 ? plan_gqa_fp8_splits(L->batch, h_q, h_kv, L->max_seq_len, sms)
+                  : plan_gqa_splits(L->batch, h_q, h_kv, L->max_seq_len, sms);
   }
   int tps = 0;
   const int eff = resolve_splits(L->max_seq_len, n_split, &tps);
@@ -256,6 +280,8 @@ int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
   p.n_split = eff;
   p.tokens_per_split = tps;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   if (eff > 1) {
     const size_t need = gqa_decode_workspace_size(L->batch, h_q, d_head, eff);
     if (!L->workspace || L->workspace_bytes < need) return DECATTN_ERR_WORKSPACE;
@@ -268,21 +294,48 @@ int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
   const bool bf16 = L->dtype == DECATTN_BF16;
   const uint64_t rows_total = static_cast<uint64_t>(L->num_blocks) * L->block_size;
   const uint32_t box_rows = static_cast<uint32_t>(L->block_size < kTile ? L->block_size : kTile);
-  const uint64_t row_bytes = static_cast<uint64_t>(h_kv) * kHeadDim * 2;
   CUtensorMap tk, tv;
-  if (!make_map_2d(&tk, k_cache, bf16, static_cast<uint64_t>(h_kv) * kHeadDim, rows_total,
-                   row_bytes, 64, box_rows) ||
-      !make_map_2d(&tv, v_cache, bf16, static_cast<uint64_t>(h_kv) * kHeadDim, rows_total,
-                   row_bytes, 64, box_rows))
-    return DECATTN_ERR_CUDA;
+  if (fp8) {
+    // One byte per element: a token's 128-d head is one 128-byte box row.
+    const uint64_t row_bytes = static_cast<uint64_t>(h_kv) * kHeadDim;
+    if (!make_map_2d_t(&tk, k_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, rows_total,
+                       row_bytes, kHeadDim, box_rows) ||
+        !make_map_2d_t(&tv, v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, rows_total,
+                       row_bytes, kHeadDim, box_rows))
+      return DECATTN_ERR_CUDA;
+  } else {
+    const uint64_t row_bytes = static_cast<uint64_t>(h_kv) * kHeadDim * 2;
+    if (!make_map_2d(&tk, k_cache, bf16, static_cast<uint64_t>(h_kv) * kHeadDim, rows_total,
+                     row_bytes, 64, box_rows) ||
+        !make_map_2d(&tv, v_cache, bf16, static_cast<uint64_t>(h_kv) * kHeadDim, rows_total,
+                     row_bytes, 64, box_rows))
+      return DECATTN_ERR_CUDA;
+  }
 
   cudaStream_t stream = static_cast<cudaStream_t>(L->stream);
-  if (launch_gqa_partial(p, tk, tv, bf16, 0, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
+  const cudaError_t e = fp8 ? launch_gqa_partial_fp8(p, tk, tv, bf16, stream)
+                            : launch_gqa_partial(p, tk, tv, bf16, 0, stream);
+  if (e != cudaSuccess) return DECATTN_ERR_CUDA;
   if (eff > 1) {
     CombineParams c{p.part_o, p.part_lse, out, L->batch * h_q, eff};
     if (launch_combine(c, kHeadDim, bf16, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
   }
   return DECATTN_OK;
+}
+
+int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_table, const int32_t* seq_lens, void* out, int h_q, int h_kv,
+               int d_head, float scale, const decattn_launch* L) {
+  return gqa_decode_impl(q, k_cache, v_cache, nullptr, nullptr, false, block_table, seq_lens, out,
+                         h_q, h_kv, d_head, scale, L);
+}
+
+int gqa_decode_fp8kv(const void* q, const void* k_cache, const void* v_cache,
+                     const float* k_scale, const float* v_scale, const int32_t* block_table,
+                     const int32_t* seq_lens, void* out, int h_q, int h_kv, int d_head,
+                     float scale, const decattn_launch* L) {
+  return gqa_decode_impl(q, k_cache, v_cache, k_scale, v_scale, true, block_table, seq_lens, out,
+                         h_q, h_kv, d_head, scale, L);
 }
 
 int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_cache,

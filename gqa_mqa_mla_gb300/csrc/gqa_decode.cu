@@ -29,6 +29,14 @@
 // Shared-memory tile layout (written by TMA with 128-byte swizzle): a stage
 // holds K then V; each is two 64-column halves of [64 tokens][128 B], and the
 // 16-byte chunk c of row r sits at chunk (c ^ (r % 8)) of that row.
+//
+// 8-bit (e4m3) caches ("Why GQA's KV Cache Savings Don't Fully Reduce TPOT",
+// "When the Serving Engineer Doesn't Get to Choose the Model Architecture":
+// an fp8 cache halves the bytes, quantised at KV-head granularity): one
+// 128-byte swizzle row holds a token's whole 128-d head, so a K or V tile is
+// [64 tokens][128 B].  The consumers build fp16 mma fragments straight from
+// those bytes (cvt e4m3x2 -> f16x2), with no staging copy; K's scale folds
+// into the score scale and V's into the output.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -52,6 +60,8 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 
 template <int G, bool kBF16>
 struct CcConsumer {
+  static constexpr int kCacheBytes = 2;
+  static constexpr int kMinBlocks = 1;
   static constexpr int kWarps = 4;
   static constexpr int kRowsPerWarp = G;
 
@@ -178,6 +188,8 @@ struct CcConsumer {
 
 template <int MT, bool kBF16>
 struct MmaConsumer {
+  static constexpr int kCacheBytes = 2;
+  static constexpr int kMinBlocks = 1;
   static constexpr int kWarps = MT <= 4 ? 4 : MT;
   static constexpr int kRowsPerWarp = 16;
   static constexpr int kWarpsPerMtile = kWarps / MT;
@@ -319,6 +331,347 @@ struct MmaConsumer {
   __device__ __forceinline__ static int slot(int w, int r) { return w * kRowsPerWarp + (r & 15); }
 };
 
+// ------------------------------------------------------------------ 8-bit cache consumers
+
+constexpr int kF8TileBytes = kTile * 128;      // [64 tokens][128 B]: K or V
+constexpr int kF8StageBytes = 2 * kF8TileBytes;  // 16 KB
+
+// Byte offset of 16-byte chunk c (0..7) of token row r in an 8-bit tile.
+__device__ __forceinline__ uint32_t f8_off(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// CUDA cores, MHA (G = 1): a half-warp holds one token row, lane chunk c
+// covers head dims 8c .. 8c + 7 (8 bytes of the row).
+template <int G, bool kBF16>
+struct CcConsumerF8 {
+  static constexpr int kCacheBytes = 1;
+  static constexpr int kMinBlocks = 1;
+  static constexpr int kWarps = 4;
+  static constexpr int kRowsPerWarp = G;
+
+  float q[G][8];
+  float o[G][8];
+  float m[G], l[G];
+  float v_scale;
+  int chunk, half, cw;
+
+  __device__ __forceinline__ void init(const GqaParams& p, int b, int j, int cw_, int lane) {
+    cw = cw_;
+    chunk = lane & 15;
+    half = lane >> 4;
+    v_scale = p.v_scale[j];
+    const uint16_t* qb = static_cast<const uint16_t*>(p.q);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const size_t row = static_cast<size_t>(b) * p.h_q + j * G + g;
+      const uint4 w = *reinterpret_cast<const uint4*>(qb + row * kHeadDim + chunk * 8);
+      const float2 a = unpack2<kBF16>(w.x), bb = unpack2<kBF16>(w.y), c = unpack2<kBF16>(w.z),
+                   d = unpack2<kBF16>(w.w);
+      q[g][0] = a.x; q[g][1] = a.y; q[g][2] = bb.x; q[g][3] = bb.y;
+      q[g][4] = c.x; q[g][5] = c.y; q[g][6] = d.x; q[g][7] = d.y;
+      m[g] = kNegInf;
+      l[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void load8(const uint8_t* tile, int r, float (&x)[8]) const {
+    const uint2 w = *reinterpret_cast<const uint2*>(tile + f8_off(r, chunk >> 1) + 8 * (chunk & 1));
+    uint32_t h[4];
+    e4m3x4_to_f16x2(w.x, h[0], h[1]);
+    e4m3x4_to_f16x2(w.y, h[2], h[3]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = unpack2<false>(h[k]);
+      x[2 * k] = f.x;
+      x[2 * k + 1] = f.y;
+    }
+  }
+
+  // Process this warp's 16 tokens (rows cw*16 .. cw*16+15) of one stage;
+  // rows >= nval are past the sequence end and are never used.
+  __device__ __forceinline__ void tile(const uint8_t* stage, int nval, float scale_log2) {
+    const uint8_t* ks = stage;
+    const uint8_t* vs = stage + kF8TileBytes;
+    float s[8][G];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = cw * 16 + 2 * i + half;
+      float k[8];
+      load8(ks, r, k);
+      float part[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(q[g][e], k[e], acc);
+        part[g] = acc;
+      }
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) s[i][g] = (r < nval) ? part[g] * scale_log2 : kNegInf;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float mt = s[0][g];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) mt = fmaxf(mt, s[i][g]);
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+      const float m_new = fmaxf(m[g], mt);
+      const float corr = (m_new == kNegInf) ? 1.f : ex2(m[g] - m_new);
+      m[g] = m_new;
+      l[g] *= corr;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[g][e] *= corr;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = cw * 16 + 2 * i + half;
+      if (r < nval) {
+        float v[8];
+        load8(vs, r, v);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pr = ex2(s[i][g] - m[g]);
+          l[g] += pr;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[g][e] = fmaf(pr, v[e], o[g][e]);
+        }
+      }
+    }
+  }
+
+  // Write this warp's (m, l, o) rows to the merge area; V's scale applies here.
+  __device__ __forceinline__ void finish(float* mo, float* mm, float* ml, int lane) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      l[g] += __shfl_xor_sync(0xffffffffu, l[g], 16);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], 16);
+    }
+    if (half == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float4* dst = reinterpret_cast<float4*>(mo + (cw * kRowsPerWarp + g) * kHeadDim + chunk * 8);
+        dst[0] = make_float4(o[g][0] * v_scale, o[g][1] * v_scale, o[g][2] * v_scale,
+                             o[g][3] * v_scale);
+        dst[1] = make_float4(o[g][4] * v_scale, o[g][5] * v_scale, o[g][6] * v_scale,
+                             o[g][7] * v_scale);
+      }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        mm[cw * kRowsPerWarp + g] = m[g];
+        ml[cw * kRowsPerWarp + g] = l[g];
+      }
+    }
+  }
+
+  __device__ __forceinline__ static int slot(int w, int r) { return w * kRowsPerWarp + r; }
+  __device__ __forceinline__ static bool covers(int /*w*/, int /*r*/) { return true; }
+};
+
+// Tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation) for
+// G >= 2 over an 8-bit cache.  The tile is read with ldmatrix treating pairs
+// of bytes as 16-bit elements.
+//   Scores: ldmatrix gives a thread 4 consecutive head dims of one token,
+//   i.e. the fp16 pairs for k-slots (2q, 2q+1) and (2q+8, 2q+9) of the B
+//   fragment once the dims inside each 16-dim k-step are ordered
+//   (4q, 4q+1 | 4q+2, 4q+3) -> slots (2q, 2q+1 | 2q+8, 2q+9).  The query's A
+//   fragments use the same order, so every dot product is unchanged.
+//   Values: transposed ldmatrix gives a thread dims (2n, 2n+1) of the two
+//   tokens of its k-slot pair; a byte permute regroups them into the token
+//   pairs of dim 2n and of dim 2n+1.  So n-tile 2b + e, column n holds head
+//   dim 16b + 2n + e; finish() writes the dims back in order.
+template <int MT, bool kBF16>
+struct MmaConsumerF8 {
+  static constexpr int kCacheBytes = 1;
+  // Three CTAs per SM: the conversion chains need more warps in flight than
+  // the 16-bit path (whose tiles are twice the bytes per token).
+  static constexpr int kMinBlocks = MT == 1 ? 3 : 1;
+  static constexpr int kWarps = MT <= 4 ? 4 : MT;
+  static constexpr int kRowsPerWarp = 16;
+  static constexpr int kWarpsPerMtile = kWarps / MT;
+  static constexpr int kTokensPerWarp = kTile / kWarpsPerMtile;
+
+  uint32_t qa[8][4];  // fp16 A fragments of the padded query group (dim order above)
+  float o[16][4];     // n-tile 2b + e, column n: head dim 16b + 2n + e
+  float m[2], l[2];
+  float v_scale;
+  int mt, tok0, cw, lane;
+
+  __device__ __forceinline__ void init(const GqaParams& p, int b, int j, int cw_, int lane_) {
+    cw = cw_;
+    lane = lane_;
+    mt = cw % MT;
+    tok0 = (cw / MT) * kTokensPerWarp;
+    v_scale = p.v_scale[j];
+    const int G = p.group;
+    const int r_lo = mt * 16 + (lane >> 2);
+    const int r_hi = r_lo + 8;
+    const int q4 = lane & 3;
+    const uint16_t* qb = static_cast<const uint16_t*>(p.q);
+    const size_t base = (static_cast<size_t>(b) * p.h_q + static_cast<size_t>(j) * G) * kHeadDim;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int d0 = ks * 16 + 4 * q4;
+      uint2 lo = make_uint2(0u, 0u), hi = make_uint2(0u, 0u);
+      if (r_lo < G) lo = *reinterpret_cast<const uint2*>(qb + base + r_lo * kHeadDim + d0);
+      if (r_hi < G) hi = *reinterpret_cast<const uint2*>(qb + base + r_hi * kHeadDim + d0);
+      const float2 l0 = unpack2<kBF16>(lo.x), l1 = unpack2<kBF16>(lo.y);
+      const float2 h0 = unpack2<kBF16>(hi.x), h1 = unpack2<kBF16>(hi.y);
+      qa[ks][0] = pack2<false>(l0.x, l0.y);
+      qa[ks][1] = pack2<false>(h0.x, h0.y);
+      qa[ks][2] = pack2<false>(l1.x, l1.y);
+      qa[ks][3] = pack2<false>(h1.x, h1.y);
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m[0] = m[1] = kNegInf;
+    l[0] = l[1] = 0.f;
+  }
+
+  __device__ __forceinline__ void tile(uint8_t* stage, int nval, float scale_log2) {
+    const uint32_t ks_base = smem_u32(stage);
+    const uint32_t vs_base = ks_base + kF8TileBytes;
+    const int q4 = lane & 3;
+#pragma unroll
+    for (int c = 0; c < kTokensPerWarp / 16; ++c) {
+      const int r0 = tok0 + 16 * c;
+      if (r0 >= nval) break;
+      if (r0 + 16 > nval) {
+        // Rows past the sequence end may hold anything (even NaN codes); zero
+        // the V rows so that P = 0 there contributes exactly nothing.
+        uint8_t* vs = stage + kF8TileBytes;
+        for (int idx = lane; idx < (r0 + 16 - nval) * 8; idx += 32) {
+          const int r = nval + (idx >> 3);
+          *reinterpret_cast<uint4*>(vs + f8_off(r, idx & 7)) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      // S = Q K^T for 16 tokens: two n-tiles of 8 tokens.  One ldmatrix.x4
+      // covers both token groups of k-steps 2w and 2w + 1.
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int mi = lane >> 3;
+        const int tok = r0 + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t k0, k1, k2, k3;  // (tokens 0-7, ks), (8-15, ks), (0-7, ks+1), (8-15, ks+1)
+          ldsm_x4(ks_base + f8_off(tok, 2 * w + (mi >> 1)), k0, k1, k2, k3);
+          uint32_t b0, b1, b2, b3;
+          e4m3x4_to_f16x2(k0, b0, b1);
+          e4m3x4_to_f16x2(k1, b2, b3);
+          mma_16816<false>(s0, qa[2 * w], b0, b1);
+          mma_16816<false>(s1, qa[2 * w], b2, b3);
+          e4m3x4_to_f16x2(k2, b0, b1);
+          e4m3x4_to_f16x2(k3, b2, b3);
+          mma_16816<false>(s0, qa[2 * w + 1], b0, b1);
+          mma_16816<false>(s1, qa[2 * w + 1], b2, b3);
+        }
+      }
+      // Scale into the log2 domain and mask tokens past the end.
+      const int ta = r0 + 2 * q4, tb = r0 + 8 + 2 * q4;
+      s0[0] = ta < nval ? s0[0] * scale_log2 : kNegInf;
+      s0[1] = ta + 1 < nval ? s0[1] * scale_log2 : kNegInf;
+      s0[2] = ta < nval ? s0[2] * scale_log2 : kNegInf;
+      s0[3] = ta + 1 < nval ? s0[3] * scale_log2 : kNegInf;
+      s1[0] = tb < nval ? s1[0] * scale_log2 : kNegInf;
+      s1[1] = tb + 1 < nval ? s1[1] * scale_log2 : kNegInf;
+      s1[2] = tb < nval ? s1[2] * scale_log2 : kNegInf;
+      s1[3] = tb + 1 < nval ? s1[3] * scale_log2 : kNegInf;
+      float mx_lo = fmaxf(fmaxf(s0[0], s0[1]), fmaxf(s1[0], s1[1]));
+      float mx_hi = fmaxf(fmaxf(s0[2], s0[3]), fmaxf(s1[2], s1[3]));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      // Every chunk holds at least one valid token, so the new maxima are finite.
+      const float mn_lo = fmaxf(m[0], mx_lo), mn_hi = fmaxf(m[1], mx_hi);
+      const float c_lo = ex2(m[0] - mn_lo), c_hi = ex2(m[1] - mn_hi);
+      m[0] = mn_lo;
+      m[1] = mn_hi;
+      l[0] *= c_lo;
+      l[1] *= c_hi;
+      // Rescale O only when some row's maximum moved (the factors are exactly
+      // 1 otherwise): after the first tiles that is rare.
+      if (__any_sync(0xffffffffu, c_lo != 1.f || c_hi != 1.f)) {
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          o[n][0] *= c_lo; o[n][1] *= c_lo; o[n][2] *= c_hi; o[n][3] *= c_hi;
+        }
+      }
+      const float p00 = ex2(s0[0] - mn_lo), p01 = ex2(s0[1] - mn_lo);
+      const float p02 = ex2(s0[2] - mn_hi), p03 = ex2(s0[3] - mn_hi);
+      const float p10 = ex2(s1[0] - mn_lo), p11 = ex2(s1[1] - mn_lo);
+      const float p12 = ex2(s1[2] - mn_hi), p13 = ex2(s1[3] - mn_hi);
+      l[0] += (p00 + p01) + (p10 + p11);
+      l[1] += (p02 + p03) + (p12 + p13);
+      const uint32_t pa[4] = {pack2<false>(p00, p01), pack2<false>(p02, p03),
+                              pack2<false>(p10, p11), pack2<false>(p12, p13)};
+      // O += P V: transposed ldmatrix per 16-dim block b and token half h
+      // gives {dims 2n, 2n+1} of tokens (2q, 2q+1) (+8 h); the permute makes
+      // the token pairs of dim 2n (low word) and dim 2n + 1 (high word).
+      {
+        const int mi = lane >> 3;
+        const int tok = r0 + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t v0, v1, v2, v3;  // (tokens 0-7, block 2w), (8-15, 2w), (0-7, 2w+1), (8-15, 2w+1)
+          ldsm_x4_trans(vs_base + f8_off(tok, 2 * w + (mi >> 1)), v0, v1, v2, v3);
+          uint32_t a0, a1, c0, c1;
+          e4m3x4_to_f16x2(byte_perm(v0, 0u, 0x3120u), a0, a1);
+          e4m3x4_to_f16x2(byte_perm(v1, 0u, 0x3120u), c0, c1);
+          mma_16816<false>(o[4 * w], pa, a0, c0);
+          mma_16816<false>(o[4 * w + 1], pa, a1, c1);
+          e4m3x4_to_f16x2(byte_perm(v2, 0u, 0x3120u), a0, a1);
+          e4m3x4_to_f16x2(byte_perm(v3, 0u, 0x3120u), c0, c1);
+          mma_16816<false>(o[4 * w + 2], pa, a0, c0);
+          mma_16816<false>(o[4 * w + 3], pa, a1, c1);
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void finish(float* mo, float* mm, float* ml, int lane_) {
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
+    const int rl = lane_ >> 2, t4 = lane_ & 3;
+    float* lo = mo + (cw * kRowsPerWarp + rl) * kHeadDim;
+    float* hi = mo + (cw * kRowsPerWarp + rl + 8) * kHeadDim;
+#pragma unroll
+    for (int bb = 0; bb < 8; ++bb) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int n = 2 * bb + e;
+        const int d0 = 16 * bb + 4 * t4 + e, d1 = d0 + 2;  // columns 2 t4 and 2 t4 + 1
+        lo[d0] = o[n][0] * v_scale;
+        lo[d1] = o[n][1] * v_scale;
+        hi[d0] = o[n][2] * v_scale;
+        hi[d1] = o[n][3] * v_scale;
+      }
+    }
+    if (t4 == 0) {
+      mm[cw * kRowsPerWarp + rl] = m[0];
+      ml[cw * kRowsPerWarp + rl] = l[0];
+      mm[cw * kRowsPerWarp + rl + 8] = m[1];
+      ml[cw * kRowsPerWarp + rl + 8] = l[1];
+    }
+  }
+
+  __device__ __forceinline__ static bool covers(int w, int r) { return (w % MT) == (r >> 4); }
+  __device__ __forceinline__ static int slot(int w, int r) { return w * kRowsPerWarp + (r & 15); }
+};
+
 // ------------------------------------------------------------------ the kernel
 
 template <class Consumer>
@@ -326,21 +679,27 @@ __host__ __device__ constexpr int merge_bytes() {
   return Consumer::kWarps * Consumer::kRowsPerWarp * (kHeadDim + 2) * 4;
 }
 
+template <class Consumer>
+__host__ __device__ constexpr int stage_bytes() {
+  return Consumer::kCacheBytes == 1 ? kF8StageBytes : kStageBytes;
+}
+
 template <class Consumer, int kStages>
 __host__ __device__ constexpr int smem_bytes() {
-  return 1024 /*alignment slack*/ + kStages * kStageBytes + 256 /*barriers*/;
+  return 1024 /*alignment slack*/ + kStages * stage_bytes<Consumer>() + 256 /*barriers*/;
 }
 
 template <class Consumer, bool kBF16, int kStages>
-__global__ void __launch_bounds__(32 * (1 + Consumer::kWarps))
+__global__ void __launch_bounds__(32 * (1 + Consumer::kWarps), Consumer::kMinBlocks)
     gqa_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const GqaParams p) {
-  static_assert(merge_bytes<Consumer>() <= kStages * kStageBytes, "merge area must fit the ring");
+  constexpr int kStage = stage_bytes<Consumer>();
+  static_assert(merge_bytes<Consumer>() <= kStages * kStage, "merge area must fit the ring");
   constexpr int kW = Consumer::kWarps;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStage);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + kStages);
   const uint32_t done_bar = smem_u32(bars + 2 * kStages);
@@ -405,16 +764,34 @@ __global__ void __launch_bounds__(32 * (1 + Consumer::kWarps))
       tma_prefetch_desc(&tm_v);
       const uint64_t policy = policy_evict_first();
       const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
-      const int x0 = j * kHeadDim;
+      const int x0 = j * kHeadDim;  // element (= byte, for an 8-bit cache) column of head j
       int issued = 0;
       for (int it = 0; it < n_tiles; ++it) {
         const int s = it % kStages;
         if (!mbar_wait(empty0 + 8 * s, ((it / kStages) & 1) ^ 1, p.err_flag)) break;
         const int t0 = t_begin + it * kTile;
         const int nval = min(kTile, t_end - t0);
-        const uint32_t st = smem_u32(smem + s * kStageBytes);
+        const uint32_t st = smem_u32(smem + s * kStage);
         const uint32_t fb = full0 + 8 * s;
-        if (bs >= kTile) {
+        if constexpr (Consumer::kCacheBytes == 1) {
+          // One 128-byte box row per token: K and V tiles of [64][128 B].
+          if (bs >= kTile) {
+            const int row = bt[t0 >> p.log2_block_size] * bs + (t0 & (bs - 1));
+            mbar_arrive_expect_tx(fb, kStage);
+            tma_load_2d_hint(st, &tm_k, x0, row, fb, policy);
+            tma_load_2d_hint(st + kF8TileBytes, &tm_v, x0, row, fb, policy);
+          } else {
+            const int nblk = (nval + bs - 1) >> p.log2_block_size;
+            const int box = bs * 128;
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nblk * 2 * box));
+            for (int k = 0; k < nblk; ++k) {
+              const int row = bt[(t0 >> p.log2_block_size) + k] * bs;
+              const uint32_t off = static_cast<uint32_t>(k * box);
+              tma_load_2d_hint(st + off, &tm_k, x0, row, fb, policy);
+              tma_load_2d_hint(st + kF8TileBytes + off, &tm_v, x0, row, fb, policy);
+            }
+          }
+        } else if (bs >= kTile) {
           const int row = bt[t0 >> p.log2_block_size] * bs + (t0 & (bs - 1));
           mbar_arrive_expect_tx(fb, kStageBytes);
           tma_load_2d_hint(st, &tm_k, x0, row, fb, policy);
@@ -448,6 +825,9 @@ __global__ void __launch_bounds__(32 * (1 + Consumer::kWarps))
   const int cw = warp - 1;
   Consumer c;
   c.init(p, b, j, cw, lane);
+  // An 8-bit cache's K scale multiplies every score of KV head j.
+  const float scale_log2 =
+      Consumer::kCacheBytes == 1 ? p.scale_log2 * p.k_scale[j] : p.scale_log2;
   bool ok = true;
   for (int it = 0; it < n_tiles; ++it) {
     const int s = it % kStages;
@@ -456,7 +836,7 @@ __global__ void __launch_bounds__(32 * (1 + Consumer::kWarps))
       break;
     }
     const int nval = min(kTile, t_end - (t_begin + it * kTile));
-    c.tile(smem + s * kStageBytes, nval, p.scale_log2);
+    c.tile(smem + s * kStage, nval, scale_log2);
     fence_proxy_async_smem();  // order any generic smem writes before the next TMA fill
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
@@ -530,7 +910,23 @@ cudaError_t dispatch(const GqaParams& p, const CUtensorMap& tk, const CUtensorMa
   return launch_one<MmaConsumer<4, kBF16>, kBF16, S>(p, tk, tv, stream);
 }
 
+template <bool kBF16>
+cudaError_t dispatch_fp8(const GqaParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                         cudaStream_t stream) {
+  constexpr int S = 4;  // 16 KB stages: keep as many cache bytes in flight as the 16-bit ring
+  if (p.group == 1) return launch_one<CcConsumerF8<1, kBF16>, kBF16, S>(p, tk, tv, stream);
+  if (p.group <= 16) return launch_one<MmaConsumerF8<1, kBF16>, kBF16, S>(p, tk, tv, stream);
+  if (p.group <= 32) return launch_one<MmaConsumerF8<2, kBF16>, kBF16, S>(p, tk, tv, stream);
+  return launch_one<MmaConsumerF8<4, kBF16>, kBF16, S>(p, tk, tv, stream);
+}
+
 }  // namespace
+
+cudaError_t launch_gqa_partial_fp8(const GqaParams& p, const CUtensorMap& tm_k,
+                                   const CUtensorMap& tm_v, bool bf16, cudaStream_t stream) {
+  return bf16 ? dispatch_fp8<true>(p, tm_k, tm_v, stream)
+              : dispatch_fp8<false>(p, tm_k, tm_v, stream);
+}
 
 cudaError_t launch_gqa_partial(const GqaParams& p, const CUtensorMap& tm_k,
                                const CUtensorMap& tm_v, bool bf16, int /*num_sms*/,

@@ -32,6 +32,8 @@ struct GqaParams {
   int block_size, log2_block_size, num_blocks, max_blocks_per_seq, max_seq_len;
   int n_split, tokens_per_split;  // tokens_per_split is a multiple of kTile
   float scale_log2;               // scale * log2(e)
+  const float* k_scale;           // [h_kv], 8-bit caches only: K value = e4m3 * k_scale[j]
+  const float* v_scale;           // [h_kv], 8-bit caches only
 };
 
 // MLA workspace (n_pairs > 1): a header of kHdrPref ints (tiles per pair,
@@ -77,6 +79,10 @@ cudaError_t launch_gqa_partial(const GqaParams& p, const CUtensorMap& tm_k,
                                cudaStream_t stream);
 // tm_out: 16-bit [B * 128, 512] output, boxes of 64 x 128; tm_po: fp32
 // [2 n_pairs * 128, 512] partials, boxes of 32 x 128 (both 128-byte swizzle).
+// The same over an e4m3 KV cache (tm_k / tm_v: 8-bit maps, boxes of 128 B x
+// min(block_size, 64) rows); q / out in fp16 or bf16.
+cudaError_t launch_gqa_partial_fp8(const GqaParams& p, const CUtensorMap& tm_k,
+                                   const CUtensorMap& tm_v, bool bf16, cudaStream_t stream);
 cudaError_t launch_mla_partial(const MlaParams& p, const CUtensorMap& tm_qa,
                                const CUtensorMap& tm_c, const CUtensorMap& tm_out,
                                const CUtensorMap& tm_po, bool bf16, cudaStream_t stream);
@@ -85,6 +91,7 @@ cudaError_t launch_mla_combine(const MlaCombineParams& p, bool bf16, cudaStream_
 
 // Planner shared by the front end and the workspace query.
 int plan_gqa_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms);
+int plan_gqa_fp8_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms);
 int plan_mla_splits(int batch, int max_seq_len, int num_sms);
 size_t mla_workspace_bytes(int batch, int n_pairs, size_t* off_lse, size_t* off_o);
 

@@ -256,6 +256,28 @@ DECATTN_DEV uint32_t pack2(float x, float y) {
   return w;
 }
 
+// Four e4m3 values packed in a word (byte 0 first) to two fp16x2 words:
+// lo = {byte 0, byte 1}, hi = {byte 2, byte 3}, the lower byte in the lower
+// half.
+DECATTN_DEV void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+DECATTN_DEV uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+DECATTN_DEV uint32_t lds32(uint32_t addr) {
+  uint32_t r;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(addr));
+  return r;
+}
+
 template <bool kBF16>
 DECATTN_DEV uint16_t round1(float x) {
   return static_cast<uint16_t>(pack2<kBF16>(x, 0.f) & 0xffffu);

@@ -178,8 +178,10 @@ def gqa_fp8_inputs(batch: int, h_q: int, h_kv: int, d_head: int = 128, seq_lens=
     g = _gen(device, seed)
     q = _randn((batch, h_q, d_head), dtype, q_std, g, device)
     shape = (nb, block_size, h_kv, d_head)
-    k = (torch.randn(shape, generator=g, device=device) * code_std).to(torch.float8_e4m3fn)
-    v = (torch.randn(shape, generator=g, device=device) * code_std).to(torch.float8_e4m3fn)
+    # torch maps magnitudes above 448 to the NaN code: clamp to the finite range first.
+    k = (torch.randn(shape, generator=g, device=device) * code_std).clamp_(-448.0, 448.0)
+    v = (torch.randn(shape, generator=g, device=device) * code_std).clamp_(-448.0, 448.0)
+    k, v = k.to(torch.float8_e4m3fn), v.to(torch.float8_e4m3fn)
     k, v = k.view(torch.uint8), v.view(torch.uint8)
     ks = (torch.rand((h_kv,), generator=g, device=device) + 0.5) / code_std
     vs = (torch.rand((h_kv,), generator=g, device=device) + 0.5) / code_std

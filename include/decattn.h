@@ -148,6 +148,28 @@ int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                        int h_kv, int d_head, float scale, const decattn_launch* launch);
 
 /*
+ * gqa_decode_fp8kv -- gqa_decode over an 8-bit KV cache ("Why GQA's KV Cache
+ * Savings Don't Fully Reduce TPOT", "When the Serving Engineer Doesn't Get to
+ * Choose the Model Architecture": an fp8 cache halves GQA's bytes per token,
+ * quantised at KV-head granularity; "07 · MHA/MQA/GQA/MLA quick learn", the
+ * question on changing the KV head count by a flag).
+ *   k_cache, v_cache  [num_blocks, block_size, h_kv, d_head] e4m3 codes, one
+ *                     byte each (1 sign, 4 exponent bits with bias 7, 3
+ *                     fraction bits; finite-only, largest magnitude 448)
+ *   k_scale, v_scale  [h_kv] fp32 device arrays: the cached value of KV head
+ *                     j is e4m3(code) * k_scale[j] (resp. v_scale[j])
+ *   q, out            [batch, h_q, d_head] in launch->dtype (fp16 / bf16)
+ * Every other argument, status and layout rule as gqa_decode (workspace
+ * sized by gqa_decode_workspace_size).  Scores and P.V run on fp16 tensor-
+ * core operands (the codes convert exactly; q is rounded to fp16) with fp32
+ * accumulation; K's scale multiplies the scores, V's the output.
+ */
+int gqa_decode_fp8kv(const void* q, const void* k_cache, const void* v_cache,
+                     const float* k_scale, const float* v_scale, const int32_t* block_table,
+                     const int32_t* seq_lens, void* out, int h_q, int h_kv, int d_head,
+                     float scale, const decattn_launch* launch);
+
+/*
  * mla_decode -- absorbed multi-head latent attention decode ("MQA, GQA, and
  * MLA", section 5; "Why GQA's KV Cache Savings Don't Fully Reduce TPOT",
  * "What Makes MLA Different").  128 heads, d_c = 512, d_rope = 64.
@@ -177,6 +199,8 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
  * queries the current device.  Returns >= 1, or a negative status. */
 int gqa_decode_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,
                            int num_sms);
+int gqa_decode_fp8kv_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,
+                                 int num_sms);
 int mla_decode_plan_splits(int batch, int max_seq_len, int num_sms);
 
 /* Workspace bytes needed for num_splits (>= 1): fp32 partial outputs and

@@ -34,6 +34,14 @@ def oracle_gqa(x: synth.GQAInputs, rows=None, scale=None):
                              scale=x.scale if scale is None else scale, rows=rows)
 
 
+def oracle_gqa_fp8(x: synth.GQAFp8Inputs, rows=None, scale=None):
+    return oracle.gqa_decode_fp8kv(synth.u16(x.q), x.k_codes.cpu().numpy(), x.v_codes.cpu().numpy(),
+                                   x.k_scale.cpu().double().numpy(), x.v_scale.cpu().double().numpy(),
+                                   x.block_table.cpu().numpy(), x.seq_lens.cpu().numpy(),
+                                   q_dtype=x.dtype, scale=x.scale if scale is None else scale,
+                                   rows=rows)
+
+
 def oracle_mla(x: synth.MLAInputs, rows=None):
     return oracle.mla_decode(synth.u16(x.q_abs), synth.u16(x.q_rope), synth.u16(x.cache),
                              x.block_table.cpu().numpy(), x.seq_lens.cpu().numpy(), dtype=x.dtype,
