@@ -185,6 +185,49 @@ def gqa_decode(q, k_cache, v_cache, block_table, seq_lens, *, dtype: str, scale:
     return out, lse
 
 
+def window_start(seq_len: int, window: int) -> int:
+    """First position a query attends to under a sliding window of `window`
+    tokens ("07 · MHA/MQA/GQA/MLA quick learn", on what sliding-window
+    attention does differently: each token sees only the last W tokens).  The
+    decode query is the sequence's newest token, already in the cache at
+    position seq_len - 1, so the window is [seq_len - window, seq_len),
+    clipped at 0."""
+    return max(0, int(seq_len) - int(window))
+
+
+def gqa_decode_window(q, k_cache, v_cache, block_table, seq_lens, *, dtype: str, scale: float,
+                      window: int, rows=None):
+    """Sliding-window GQA decode in fp64: the plain GQA definition
+    (gqa_decode) over positions [window_start(L_b, window), L_b) of each
+    sequence b.  Same arguments and results as gqa_decode."""
+    if window < 1:
+        raise ValueError("window must be >= 1")
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, h_q = np.shape(q)[0], np.shape(q)[1]
+    if rows is None:
+        rows = np.stack(np.meshgrid(np.arange(B), np.arange(h_q), indexing="ij"), -1).reshape(-1, 2)
+    rows = np.asarray(rows, dtype=np.int32).reshape(-1, 2)
+    d = np.shape(q)[2]
+    out = np.empty((rows.shape[0], d), dtype=np.float64)
+    lse = np.empty((rows.shape[0],), dtype=np.float64)
+    for b in np.unique(rows[:, 0]):
+        sel = np.nonzero(rows[:, 0] == b)[0]
+        o, l = gqa_decode(q, k_cache, v_cache, block_table, sl, dtype=dtype, scale=scale,
+                          rows=rows[sel], t_begin=window_start(sl[b], window), t_end=-1)
+        out[sel], lse[sel] = o, l
+    return out, lse
+
+
+def gqa_decode_fp8kv_window(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens, *,
+                            q_dtype: str, scale: float, window: int, rows=None):
+    """Sliding-window decode over an e4m3 KV cache: dequantise (as in
+    gqa_decode_fp8kv), then gqa_decode_window."""
+    q64 = half_to_double(q) if q_dtype == "fp16" else bf16_to_double(q)
+    return gqa_decode_window(q64, dequant_e4m3(k_codes, k_scale), dequant_e4m3(v_codes, v_scale),
+                             block_table, seq_lens, dtype="f64", scale=scale, window=window,
+                             rows=rows)
+
+
 def mla_decode(q_abs, q_rope, cache, block_table, seq_lens, *, dtype: str, scale: float,
                rows=None, t_begin: int = 0, t_end: int = -1):
     """Absorbed MLA decode in fp64.

@@ -467,3 +467,144 @@ def test_fp8kv_scales_act_on_scores_and_values_per_kv_head():
     heads = np.tile(np.arange(q.shape[1]), q.shape[0])
     np.testing.assert_allclose(o, o_ref * vs[heads // G][:, None], rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(lse, lse_ref, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- sliding-window decode
+
+def _window_case(seed, lens, bs=4, h_q=4, h_kv=2, d=8):
+    rng = np.random.default_rng(seed)
+    B = len(lens)
+    per = max(math.ceil(max(lens) / bs), 1)
+    nb = B * per + 3
+    k = rng.standard_normal((nb, bs, h_kv, d)) * 1.5
+    v = rng.standard_normal((nb, bs, h_kv, d))
+    q = rng.standard_normal((B, h_q, d))
+    bt = rng.permutation(nb)[:B * per].reshape(B, per).astype(np.int32)
+    return q, k, v, bt, np.array(lens, np.int32)
+
+
+def test_window_start_reading():
+    # the window holds the newest `window` positions, the query's own included
+    assert oracle.window_start(10, 3) == 7
+    assert oracle.window_start(10, 10) == 0
+    assert oracle.window_start(10, 11) == 0
+    assert oracle.window_start(0, 1) == 0
+    assert oracle.window_start(5, 1) == 4
+
+
+def test_window_covering_every_sequence_is_full_attention():
+    q, k, v, bt, sl = _window_case(20, [13, 1, 0, 9])
+    full, lf = _gqa(q, k, v, bt, sl, 0.4)
+    for w in (13, 14, 1000):
+        o, l = oracle.gqa_decode_window(q, k, v, bt, sl, dtype="f64", scale=0.4, window=w)
+        assert np.array_equal(o, full) and np.array_equal(l, lf)
+
+
+def test_window_of_one_returns_the_newest_value():
+    q, k, v, bt, sl = _window_case(21, [13, 1, 7])
+    o, l = oracle.gqa_decode_window(q, k, v, bt, sl, dtype="f64", scale=0.4, window=1)
+    bs, group = k.shape[1], q.shape[1] // k.shape[2]
+    for b, L in enumerate(sl):
+        t = L - 1
+        blk, slot = bt[b, t // bs], t % bs
+        for i in range(q.shape[1]):
+            r = b * q.shape[1] + i
+            assert np.array_equal(o[r], v[blk, slot, i // group])
+            assert l[r] == pytest.approx(0.4 * float(q[b, i] @ k[blk, slot, i // group]), abs=1e-13)
+
+
+@pytest.mark.parametrize("window", [2, 3, 4, 5, 8, 11])
+def test_window_equals_full_attention_on_the_last_tokens_copied_out(window):
+    """Copy each sequence's last `window` tokens into a fresh contiguous cache
+    and attend to all of them: the windowed result must be the same, and one
+    token more or fewer must not be."""
+    q, k, v, bt, sl = _window_case(22, [13, 6, 12, 4, 5])
+    bs = k.shape[1]
+    o, l = oracle.gqa_decode_window(q, k, v, bt, sl, dtype="f64", scale=0.7, window=window)
+
+    def copied(b, n):
+        L = int(sl[b])
+        pos = list(range(max(0, L - n), L))
+        kk = np.stack([k[bt[b, t // bs], t % bs] for t in pos])[None]  # one block of len(pos)
+        vv = np.stack([v[bt[b, t // bs], t % bs] for t in pos])[None]
+        return _gqa(q[b:b + 1], kk, vv, np.zeros((1, 1), np.int32),
+                    np.array([len(pos)], np.int32), 0.7)
+
+    h_q = q.shape[1]
+    for b in range(len(sl)):
+        ref_o, ref_l = copied(b, window)
+        got = slice(b * h_q, (b + 1) * h_q)
+        np.testing.assert_allclose(o[got], ref_o, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l[got], ref_l, rtol=0, atol=1e-13)
+        if sl[b] > window:  # sensitivity: an off-by-one window is a different result
+            assert not np.allclose(o[got], copied(b, window + 1)[0])
+            assert not np.allclose(o[got], copied(b, window - 1)[0])
+
+
+def test_growing_the_window_by_one_admits_exactly_the_next_older_token():
+    """out_{W+1} and lse_{W+1} follow from out_W, lse_W and the one token at
+    position L - W - 1 by the closed-form softmax update."""
+    q, k, v, bt, sl = _window_case(23, [13, 9])
+    bs, h_q, group = k.shape[1], q.shape[1], q.shape[1] // k.shape[2]
+    scale = 0.6
+    for w in (1, 3, 6):
+        o1, l1 = oracle.gqa_decode_window(q, k, v, bt, sl, dtype="f64", scale=scale, window=w)
+        o2, l2 = oracle.gqa_decode_window(q, k, v, bt, sl, dtype="f64", scale=scale, window=w + 1)
+        for b, L in enumerate(sl):
+            t = L - w - 1
+            blk, slot = bt[b, t // bs], t % bs
+            for i in range(h_q):
+                r = b * h_q + i
+                s = scale * float(q[b, i] @ k[blk, slot, i // group])
+                lse = np.logaddexp(l1[r], s)
+                assert l2[r] == pytest.approx(lse, abs=1e-12)
+                expect = math.exp(l1[r] - lse) * o1[r] + math.exp(s - lse) * v[blk, slot, i // group]
+                np.testing.assert_allclose(o2[r], expect, rtol=0, atol=1e-12)
+
+
+def test_blocks_before_the_window_are_never_read():
+    """Blocks wholly before the window may be recycled: invalid ids there and
+    NaN in the window's first block before its start change nothing."""
+    q, k, v, bt, sl = _window_case(24, [13, 11], bs=4)
+    w = 6
+    ref, lref = oracle.gqa_decode_window(q, k, v, bt, sl, dtype="f64", scale=0.5, window=w)
+    bt2, k2, v2 = bt.copy(), k.copy(), v.copy()
+    for b, L in enumerate(sl):
+        w0 = oracle.window_start(L, w)
+        for t in range(w0):
+            blk = bt[b, t // 4]
+            k2[blk, t % 4] = np.nan
+            v2[blk, t % 4] = np.nan
+        bt2[b, :w0 // 4] = -1  # blocks wholly before the window
+    o, l = oracle.gqa_decode_window(q, k2, v2, bt2, sl, dtype="f64", scale=0.5, window=w)
+    assert np.array_equal(o, ref) and np.array_equal(l, lref)
+    with pytest.raises(ValueError):  # but a bad id inside the window is still an error
+        bt3 = bt.copy()
+        bt3[0, (int(sl[0]) - 1) // 4] = 99
+        oracle.gqa_decode_window(q, k, v, bt3, sl, dtype="f64", scale=0.5, window=w)
+
+
+def test_fp8kv_window_reduces_to_the_full_fp8_path_and_to_one_value():
+    rng = np.random.default_rng(25)
+    nb, bs, h_kv, d, h_q = 6, 4, 2, 8, 4
+    codes_k = rng.integers(0, 256, (nb, bs, h_kv, d), dtype=np.uint8)
+    codes_v = rng.integers(0, 256, (nb, bs, h_kv, d), dtype=np.uint8)
+    codes_k[(codes_k & 0x7F) == 0x7F] = 0x10  # no NaN codes
+    codes_v[(codes_v & 0x7F) == 0x7F] = 0x20
+    ks, vs = np.array([0.01, 0.02]), np.array([0.5, 0.25])
+    q = torch.randn(2, h_q, d, generator=torch.Generator().manual_seed(5)).to(torch.float16)
+    qb = q.view(torch.int16).numpy().view(np.uint16)
+    bt = np.array([[0, 1, 2], [3, 4, 5]], np.int32)
+    sl = np.array([11, 7], np.int32)
+    full = oracle.gqa_decode_fp8kv(qb, codes_k, codes_v, ks, vs, bt, sl, q_dtype="fp16", scale=0.3)
+    win = oracle.gqa_decode_fp8kv_window(qb, codes_k, codes_v, ks, vs, bt, sl, q_dtype="fp16",
+                                         scale=0.3, window=11)
+    assert np.array_equal(full[0], win[0])
+    one, _ = oracle.gqa_decode_fp8kv_window(qb, codes_k, codes_v, ks, vs, bt, sl, q_dtype="fp16",
+                                            scale=0.3, window=1)
+    for b, L in enumerate(sl):
+        t = L - 1
+        for i in range(h_q):
+            j = i // 2
+            expect = oracle.e4m3_to_double(codes_v[bt[b, t // bs], t % bs, j]) * vs[j]
+            assert np.array_equal(one[b * h_q + i], expect)
