@@ -41,6 +41,7 @@ METRIC = "decode-attn KV-read GB/s (% of GB300 HBM peak) and decode steps/s per 
 GQA_WORKLOAD = "llama3_70b_b64_s8k"
 MLA_WORKLOAD = "deepseek_v2_mla_b32_s8k"
 GQA_FP8_WORKLOAD = "llama3_70b_b64_s8k_fp8"
+GQA_WINDOW = 4096  # sliding-window extra: the 70B-shaped layer attending to its last 4096 tokens
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GQA_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/gqa_decode.cu", "gqa_mqa_mla_gb300/csrc/ptx.cuh",
                       "gqa_mqa_mla_gb300/csrc/internal.h"]
@@ -61,6 +62,14 @@ def gqa_fp8_bytes(x) -> int:
     return kv + 2 * x.batch * x.h_q * x.d_head * 2 + 2 * x.h_kv * 4
 
 
+def gqa_window_bytes(x, window: int) -> int:
+    """Cache bytes a sliding window attends to (min(L_b, window) tokens per
+    sequence) plus q and out."""
+    e = 2
+    toks = int(torch.clamp(x.seq_lens, max=window).sum().item())
+    return toks * x.h_kv * x.d_head * 2 * e + 2 * x.batch * x.h_q * x.d_head * e
+
+
 def mla_bytes(x) -> int:
     e = 2
     return (x.batch * 128 * 576 * e + int(x.seq_lens.sum().item()) * 576 * e
@@ -69,6 +78,22 @@ def mla_bytes(x) -> int:
 
 def mla_flops(x) -> int:
     return int(x.seq_lens.sum().item()) * 128 * (2 * 576 + 2 * 512)
+
+
+def time_calls(call, n: int, stream, dev) -> float:
+    """Mean ms per call of n back-to-back calls on `stream` after 5 warm-ups
+    (CUDA events on the launching stream, synchronised on both sides)."""
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / n
 
 
 def load_peaks():
@@ -452,18 +477,8 @@ def main():
                                 max_seq_len=fx.max_seq_len, out=f_out, num_splits=f_ns,
                                 workspace=f_ws, err_flag=flag)
 
-        for _ in range(5):
-            f_call()
-        torch.cuda.synchronize(dev)
         nf = max(3, min(K, 500))
-        f0 = torch.cuda.Event(enable_timing=True)
-        f1 = torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(nf):
-            f_call()
-        f1.record(stream)
-        torch.cuda.synchronize(dev)
-        f_ms = f0.elapsed_time(f1) / nf
+        f_ms = time_calls(f_call, nf, stream, dev)
         fb = gqa_fp8_bytes(fx)
         f_gbps = fb / (f_ms * 1e-3) / 1e9
         extras = {"gqa_fp8": {"workload": GQA_FP8_WORKLOAD, "GBps": f_gbps, "ms": f_ms,
@@ -472,6 +487,29 @@ def main():
                               "cache_dtype": "e4m3 (per-KV-head fp32 scales)"}}
         err |= int(flag.item())
         del fx, f_ws, f_out
+
+        # The 16-bit 70B-shaped layer under a sliding window: every sequence
+        # attends to its last GQA_WINDOW tokens only.
+        w_ns = da.gqa_window_plan_splits(gx.batch, gx.h_q, gx.h_kv, gx.max_seq_len, GQA_WINDOW,
+                                         gx.block_size)
+        w_ws = torch.empty(max(16, da.gqa_workspace_size(gx.batch, gx.h_q, w_ns)),
+                           dtype=torch.uint8, device=dev)
+        w_out = torch.empty_like(gx.q)
+
+        def w_call():
+            da.gqa_decode_window(gx.q, gx.k_cache, gx.v_cache, gx.block_table, gx.seq_lens,
+                                 window=GQA_WINDOW, scale=gx.scale, max_seq_len=gx.max_seq_len,
+                                 out=w_out, num_splits=w_ns, workspace=w_ws, err_flag=flag)
+
+        w_ms = time_calls(w_call, nf, stream, dev)
+        wb = gqa_window_bytes(gx, GQA_WINDOW)
+        w_gbps = wb / (w_ms * 1e-3) / 1e9
+        extras["gqa_window"] = {"workload": f"{GQA_WORKLOAD} window {GQA_WINDOW}",
+                                "GBps": w_gbps, "ms": w_ms, "steps_per_s": 1e3 / w_ms,
+                                "bytes": wb, "steps": nf, "frac_of_hbm_peak": w_gbps / hbm,
+                                "splits": w_ns}
+        err |= int(flag.item())
+        del w_ws, w_out
 
     parts_out = {}
     for name, ms in part_ms.items():

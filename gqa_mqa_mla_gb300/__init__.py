@@ -1,7 +1,8 @@
 """libdecattn: GB300-native single-token decode attention over a paged KV cache.
 
-MHA / GQA / MQA (``gqa_decode``, and ``gqa_decode_fp8kv`` over an 8-bit e4m3 KV
-cache) and absorbed MLA (``mla_decode``), hand-written
+MHA / GQA / MQA (``gqa_decode``, ``gqa_decode_fp8kv`` over an 8-bit e4m3 KV
+cache, and their sliding-window forms ``gqa_decode_window`` /
+``gqa_decode_fp8kv_window``) and absorbed MLA (``mla_decode``), hand-written
 CUDA kernels for sm_103a behind a C ABI (include/decattn.h).  This package is
 the thin Python binding; ``synth`` draws seeded synthetic inputs.
 """
@@ -12,8 +13,11 @@ from .binding import (  # noqa: F401
     FLAG_TIMEOUT,
     gqa_decode,
     gqa_decode_fp8kv,
+    gqa_decode_fp8kv_window,
+    gqa_decode_window,
     gqa_fp8_plan_splits,
     gqa_plan_splits,
+    gqa_window_plan_splits,
     gqa_workspace_size,
     kv_bytes_per_token,
     lib,

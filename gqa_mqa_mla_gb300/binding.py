@@ -79,6 +79,12 @@ def lib() -> ctypes.CDLL:
             L.gqa_decode.restype = I
             L.gqa_decode_fp8kv.argtypes = [P, P, P, P, P, P, P, P, I, I, I, F, LP]
             L.gqa_decode_fp8kv.restype = I
+            L.gqa_decode_window.argtypes = [P, P, P, P, P, P, I, I, I, F, I, LP]
+            L.gqa_decode_window.restype = I
+            L.gqa_decode_fp8kv_window.argtypes = [P, P, P, P, P, P, P, P, I, I, I, F, I, LP]
+            L.gqa_decode_fp8kv_window.restype = I
+            L.gqa_decode_window_plan_splits.argtypes = [I, I, I, I, I, I, I, I, I]
+            L.gqa_decode_window_plan_splits.restype = I
             L.mla_decode.argtypes = [P, P, P, P, P, P, F, LP]
             L.mla_decode.restype = I
             L.gqa_decode_plan_splits.argtypes = [I, I, I, I, I, I]
@@ -131,6 +137,16 @@ def gqa_fp8_plan_splits(batch: int, h_q: int, h_kv: int, max_seq_len: int, d_hea
     return r
 
 
+def gqa_window_plan_splits(batch: int, h_q: int, h_kv: int, max_seq_len: int, window: int,
+                           block_size: int, kv_bytes: int = 2, d_head: int = 128,
+                           num_sms: int = 0) -> int:
+    r = lib().gqa_decode_window_plan_splits(batch, h_q, h_kv, d_head, max_seq_len, window,
+                                            block_size, kv_bytes, num_sms)
+    if r < 0:
+        raise DecAttnError("gqa_decode_window_plan_splits", r)
+    return r
+
+
 def mla_plan_splits(batch: int, max_seq_len: int, num_sms: int = 0) -> int:
     r = lib().mla_decode_plan_splits(batch, max_seq_len, num_sms)
     if r < 0:
@@ -174,13 +190,15 @@ def make_launch(batch, num_blocks, block_size, max_blocks_per_seq, max_seq_len, 
 
 
 def gqa_decode(q, k_cache, v_cache, block_table, seq_lens, *, scale: float, max_seq_len: int,
-               out=None, num_splits: int = 0, workspace=None, err_flag=None, stream=None):
+               out=None, num_splits: int = 0, workspace=None, err_flag=None, stream=None,
+               window: int | None = None):
     """MHA/GQA/MQA decode through the C ABI; returns out [B, h_q, d].
 
     q [B, h_q, d]; k_cache/v_cache [num_blocks, block_size, h_kv, d];
     block_table int32 [B, max_blocks]; seq_lens int32 [B]; max_seq_len a host
     upper bound of seq_lens.  workspace: optional uint8 CUDA tensor (sized by
-    gqa_workspace_size); allocated here when needed and not given.
+    gqa_workspace_size); allocated here when needed and not given.  window:
+    attend only to each sequence's last `window` tokens (gqa_decode_window).
     """
     _check(q, "q", ndim=3)
     _check(k_cache, "k_cache", q.dtype, 4)
@@ -197,29 +215,44 @@ def gqa_decode(q, k_cache, v_cache, block_table, seq_lens, *, scale: float, max_
         raise ValueError(f"h_q={h_q} is not a multiple of h_kv={h_kv}")
     if out is None:
         out = torch.empty_like(q)
-    ns = num_splits if num_splits else gqa_plan_splits(B, h_q, h_kv, max_seq_len, d)
+    if num_splits:
+        ns = num_splits
+    elif window is None:
+        ns = gqa_plan_splits(B, h_q, h_kv, max_seq_len, d)
+    else:
+        ns = gqa_window_plan_splits(B, h_q, h_kv, max_seq_len, window, bs, 2, d)
     need = gqa_workspace_size(B, h_q, ns, d)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     L = make_launch(B, nb, bs, block_table.shape[1], max_seq_len, ns, _DT[q.dtype],
                     _ptr(workspace), 0 if workspace is None else workspace.numel(),
                     _ptr(err_flag), _stream_handle(stream))
-    st = lib().gqa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                          block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(), h_q, h_kv,
-                          d, float(scale), ctypes.byref(L))
+    args = (q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+            seq_lens.data_ptr(), out.data_ptr(), h_q, h_kv, d, float(scale))
+    if window is None:
+        name, st = "gqa_decode", lib().gqa_decode(*args, ctypes.byref(L))
+    else:
+        name = "gqa_decode_window"
+        st = lib().gqa_decode_window(*args, int(window), ctypes.byref(L))
     if st != DECATTN_OK:
-        raise DecAttnError("gqa_decode", st)
+        raise DecAttnError(name, st)
     return out
+
+
+def gqa_decode_window(q, k_cache, v_cache, block_table, seq_lens, *, window: int, **kw):
+    """gqa_decode restricted to each sequence's last `window` tokens."""
+    return gqa_decode(q, k_cache, v_cache, block_table, seq_lens, window=window, **kw)
 
 
 def gqa_decode_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens, *,
                      scale: float, max_seq_len: int, out=None, num_splits: int = 0,
-                     workspace=None, err_flag=None, stream=None):
+                     workspace=None, err_flag=None, stream=None, window: int | None = None):
     """GQA decode over an 8-bit (e4m3) KV cache through the C ABI; returns out.
 
     q [B, h_q, d] fp16/bf16; k_codes/v_codes uint8 (or float8_e4m3fn)
     [num_blocks, block_size, h_kv, d]; k_scale/v_scale float32 [h_kv] (the
-    value of KV head j is e4m3(code) * scale[j]); the rest as gqa_decode.
+    value of KV head j is e4m3(code) * scale[j]); the rest as gqa_decode
+    (window: gqa_decode_fp8kv_window).
     """
     _check(q, "q", ndim=3)
     if q.dtype not in _DT:
@@ -244,20 +277,36 @@ def gqa_decode_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_len
         raise ValueError(f"h_q={h_q} is not a multiple of h_kv={h_kv}")
     if out is None:
         out = torch.empty_like(q)
-    ns = num_splits if num_splits else gqa_fp8_plan_splits(B, h_q, h_kv, max_seq_len, d)
+    if num_splits:
+        ns = num_splits
+    elif window is None:
+        ns = gqa_fp8_plan_splits(B, h_q, h_kv, max_seq_len, d)
+    else:
+        ns = gqa_window_plan_splits(B, h_q, h_kv, max_seq_len, window, bs, 1, d)
     need = gqa_workspace_size(B, h_q, ns, d)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     L = make_launch(B, nb, bs, block_table.shape[1], max_seq_len, ns, _DT[q.dtype],
                     _ptr(workspace), 0 if workspace is None else workspace.numel(),
                     _ptr(err_flag), _stream_handle(stream))
-    st = lib().gqa_decode_fp8kv(q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
-                                k_scale.data_ptr(), v_scale.data_ptr(), block_table.data_ptr(),
-                                seq_lens.data_ptr(), out.data_ptr(), h_q, h_kv, d, float(scale),
-                                ctypes.byref(L))
+    args = (q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(), k_scale.data_ptr(),
+            v_scale.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
+            h_q, h_kv, d, float(scale))
+    if window is None:
+        name, st = "gqa_decode_fp8kv", lib().gqa_decode_fp8kv(*args, ctypes.byref(L))
+    else:
+        name = "gqa_decode_fp8kv_window"
+        st = lib().gqa_decode_fp8kv_window(*args, int(window), ctypes.byref(L))
     if st != DECATTN_OK:
-        raise DecAttnError("gqa_decode_fp8kv", st)
+        raise DecAttnError(name, st)
     return out
+
+
+def gqa_decode_fp8kv_window(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens, *,
+                            window: int, **kw):
+    """gqa_decode_fp8kv restricted to each sequence's last `window` tokens."""
+    return gqa_decode_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens,
+                            window=window, **kw)
 
 
 def mla_decode(q_absorbed, q_rope, latent_cache, block_table, seq_lens, *, scale: float,

@@ -86,6 +86,15 @@ int resolve_splits(int max_seq_len, int n_split, int* tokens_per_split) {
   return (tiles + tiles_per - 1) / tiles_per;
 }
 
+// A sliding window of W tokens starts at a block (or 64-token) boundary at
+// most min(block_size, 64) - 1 tokens before the window: the longest token
+// range any sequence streams.
+int window_span(int max_seq_len, int window, int block_size) {
+  if (window <= 0) return max_seq_len;
+  const int64_t span = static_cast<int64_t>(window) + (block_size < kTile ? block_size : kTile) - 1;
+  return span < max_seq_len ? static_cast<int>(span) : max_seq_len;
+}
+
 // Split count for `units` independent (sequence[, KV head]) work units on
 // `slots` resident CTAs.  The kernels stream HBM, so one split per unit is
 // best once there are enough CTAs to keep every SM fed (measured: the
@@ -207,6 +216,18 @@ int gqa_decode_fp8kv_plan_splits(int batch, int h_q, int h_kv, int d_head, int m
   return plan_gqa_fp8_splits(batch, h_q, h_kv, max_seq_len, num_sms);
 }
 
+int gqa_decode_window_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,
+                                  int window, int block_size, int kv_bytes, int num_sms) {
+  if (batch < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 || d_head < 1 || max_seq_len < 0 ||
+      window < 1 || !is_pow2(block_size) || (kv_bytes != 1 && kv_bytes != 2))
+    return DECATTN_ERR_INVALID_ARG;
+  if (num_sms <= 0) num_sms = device_sm_count();
+  if (num_sms <= 0) return DECATTN_ERR_CUDA;
+  const int span = window_span(max_seq_len, window, block_size);
+  return kv_bytes == 1 ? plan_gqa_fp8_splits(batch, h_q, h_kv, span, num_sms)
+                       : plan_gqa_splits(batch, h_q, h_kv, span, num_sms);
+}
+
 int mla_decode_plan_splits(int batch, int max_seq_len, int num_sms) {
   if (batch < 1 || max_seq_len < 0) return DECATTN_ERR_INVALID_ARG;
   if (num_sms <= 0) num_sms = device_sm_count();
@@ -237,7 +258,8 @@ static int check_launch(const decattn_launch* L, bool mla) {
 static int gqa_decode_impl(const void* q, const void* k_cache, const void* v_cache,
                            const float* k_scale, const float* v_scale, bool fp8,
                            const int32_t* block_table, const int32_t* seq_lens, void* out,
-                           int h_q, int h_kv, int d_head, float scale, const decattn_launch* L) {
+                           int h_q, int h_kv, int d_head, float scale, int window,
+                           const decattn_launch* L) {
   int st = check_launch(L, false);
   if (st != DECATTN_OK) return st;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
@@ -252,15 +274,17 @@ static int gqa_decode_impl(const void* q, const void* k_cache, const void* v_cac
   if (d_head != kHeadDim) return DECATTN_ERR_UNSUPPORTED;
   if (h_q / h_kv > 64) return DECATTN_ERR_UNSUPPORTED;
 
+  if (window < 0) return DECATTN_ERR_INVALID_ARG;
+  const int span = window_span(L->max_seq_len, window, L->block_size);
   int n_split = L->num_splits;
   if (n_split == 0) {
     const int sms = device_sm_count();
     if (sms <= 0) return DECATTN_ERR_CUDA;
-    n_split = fp8 ? plan_gqa_fp8_splits(L->batch, h_q, h_kv, L->max_seq_len, sms)
-                  : plan_gqa_splits(L->batch, h_q, h_kv, L->max_seq_len, sms);
+    n_split = fp8 ? plan_gqa_fp8_splits(L->batch, h_q, h_kv, span, sms)
+                  : plan_gqa_splits(L->batch, h_q, h_kv, span, sms);
   }
   int tps = 0;
-  const int eff = resolve_splits(L->max_seq_len, n_split, &tps);
+  const int eff = resolve_splits(span, n_split, &tps);
 
   GqaParams p{};
   p.q = q;
@@ -280,6 +304,7 @@ static int gqa_decode_impl(const void* q, const void* k_cache, const void* v_cac
   p.n_split = eff;
   p.tokens_per_split = tps;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.window = window;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   if (eff > 1) {
@@ -327,7 +352,7 @@ int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_table, const int32_t* seq_lens, void* out, int h_q, int h_kv,
                int d_head, float scale, const decattn_launch* L) {
   return gqa_decode_impl(q, k_cache, v_cache, nullptr, nullptr, false, block_table, seq_lens, out,
-                         h_q, h_kv, d_head, scale, L);
+                         h_q, h_kv, d_head, scale, 0, L);
 }
 
 int gqa_decode_fp8kv(const void* q, const void* k_cache, const void* v_cache,
@@ -335,7 +360,25 @@ int gqa_decode_fp8kv(const void* q, const void* k_cache, const void* v_cache,
                      const int32_t* seq_lens, void* out, int h_q, int h_kv, int d_head,
                      float scale, const decattn_launch* L) {
   return gqa_decode_impl(q, k_cache, v_cache, k_scale, v_scale, true, block_table, seq_lens, out,
-                         h_q, h_kv, d_head, scale, L);
+                         h_q, h_kv, d_head, scale, 0, L);
+}
+
+int gqa_decode_window(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* seq_lens, void* out, int h_q,
+                      int h_kv, int d_head, float scale, int window, const decattn_launch* L) {
+  if (window < 1) return DECATTN_ERR_INVALID_ARG;
+  return gqa_decode_impl(q, k_cache, v_cache, nullptr, nullptr, false, block_table, seq_lens, out,
+                         h_q, h_kv, d_head, scale, window, L);
+}
+
+int gqa_decode_fp8kv_window(const void* q, const void* k_cache, const void* v_cache,
+                            const float* k_scale, const float* v_scale,
+                            const int32_t* block_table, const int32_t* seq_lens, void* out,
+                            int h_q, int h_kv, int d_head, float scale, int window,
+                            const decattn_launch* L) {
+  if (window < 1) return DECATTN_ERR_INVALID_ARG;
+  return gqa_decode_impl(q, k_cache, v_cache, k_scale, v_scale, true, block_table, seq_lens, out,
+                         h_q, h_kv, d_head, scale, window, L);
 }
 
 int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_cache,

@@ -98,8 +98,10 @@ struct CcConsumer {
   }
 
   // Process this warp's 16 tokens (rows cw*16 .. cw*16+15) of one stage;
-  // rows >= nval are past the sequence end and are never used.
-  __device__ __forceinline__ void tile(const uint8_t* stage, int nval, float scale_log2) {
+  // rows >= nval are past the sequence end and rows < nskip before a sliding
+  // window: neither is used.
+  __device__ __forceinline__ void tile(const uint8_t* stage, int nskip, int nval, float scale_log2) {
+    const unsigned span = static_cast<unsigned>(nval - nskip);  // nskip < nval
     const uint8_t* ks = stage;
     const uint8_t* vs = stage + kKvTileBytes;
     float s[8][G];
@@ -121,8 +123,9 @@ struct CcConsumer {
 #pragma unroll
         for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
       }
+      const bool live = static_cast<unsigned>(r - nskip) < span;
 #pragma unroll
-      for (int g = 0; g < G; ++g) s[i][g] = (r < nval) ? part[g] * scale_log2 : kNegInf;
+      for (int g = 0; g < G; ++g) s[i][g] = live ? part[g] * scale_log2 : kNegInf;
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -140,7 +143,7 @@ struct CcConsumer {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = cw * 16 + 2 * i + half;
-      if (r < nval) {
+      if (static_cast<unsigned>(r - nskip) < span) {
         float v[8];
         load8(vs + tile_off(r, chunk), v);
 #pragma unroll
@@ -225,7 +228,8 @@ struct MmaConsumer {
     l[0] = l[1] = 0.f;
   }
 
-  __device__ __forceinline__ void tile(uint8_t* stage, int nval, float scale_log2) {
+  __device__ __forceinline__ void tile(uint8_t* stage, int nskip, int nval, float scale_log2) {
+    const unsigned span = static_cast<unsigned>(nval - nskip);  // nskip < nval
     const uint32_t ks_base = smem_u32(stage);
     const uint32_t vs_base = ks_base + kKvTileBytes;
     const int t4 = lane & 3;
@@ -233,12 +237,16 @@ struct MmaConsumer {
     for (int c = 0; c < kTokensPerWarp / 16; ++c) {
       const int r0 = tok0 + 16 * c;
       if (r0 >= nval) break;
-      if (r0 + 16 > nval) {
-        // Rows past the sequence end may hold anything (even NaN); zero the
-        // V rows so that P = 0 there contributes exactly nothing.
+      if (r0 + 16 <= nskip) continue;  // wholly before a sliding window
+      if (r0 + 16 > nval || r0 < nskip) {
+        // Rows past the sequence end (or before a sliding window) may hold
+        // anything, even NaN; zero their V rows so that P = 0 there
+        // contributes exactly nothing.  Both ranges are under 16 rows.
         uint8_t* vs = stage + kKvTileBytes;
-        for (int idx = lane; idx < (r0 + 16 - nval) * 16; idx += 32) {
-          const int r = nval + (idx >> 4);
+        const int lo = max(0, nskip - r0), hi = max(0, r0 + 16 - nval);
+        for (int idx = lane; idx < (lo + hi) * 16; idx += 32) {
+          const int k = idx >> 4;
+          const int r = k < lo ? r0 + k : nval + (k - lo);
           *reinterpret_cast<uint4*>(vs + tile_off(r, idx & 15)) = make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
@@ -256,16 +264,17 @@ struct MmaConsumer {
           mma_16816<kBF16>(s1, qa[ks], b2, b3);
         }
       }
-      // Scale into the log2 domain and mask tokens past the end.
-      const int ta = r0 + 2 * t4, tb = r0 + 8 + 2 * t4;
-      s0[0] = ta < nval ? s0[0] * scale_log2 : kNegInf;
-      s0[1] = ta + 1 < nval ? s0[1] * scale_log2 : kNegInf;
-      s0[2] = ta < nval ? s0[2] * scale_log2 : kNegInf;
-      s0[3] = ta + 1 < nval ? s0[3] * scale_log2 : kNegInf;
-      s1[0] = tb < nval ? s1[0] * scale_log2 : kNegInf;
-      s1[1] = tb + 1 < nval ? s1[1] * scale_log2 : kNegInf;
-      s1[2] = tb < nval ? s1[2] * scale_log2 : kNegInf;
-      s1[3] = tb + 1 < nval ? s1[3] * scale_log2 : kNegInf;
+      // Scale into the log2 domain and mask tokens outside [nskip, nval).
+      // ta, tb count from the window start: valid rows are [0, span).
+      const int ta = r0 - nskip + 2 * t4, tb = ta + 8;
+      s0[0] = static_cast<unsigned>(ta) < span ? s0[0] * scale_log2 : kNegInf;
+      s0[1] = static_cast<unsigned>(ta + 1) < span ? s0[1] * scale_log2 : kNegInf;
+      s0[2] = static_cast<unsigned>(ta) < span ? s0[2] * scale_log2 : kNegInf;
+      s0[3] = static_cast<unsigned>(ta + 1) < span ? s0[3] * scale_log2 : kNegInf;
+      s1[0] = static_cast<unsigned>(tb) < span ? s1[0] * scale_log2 : kNegInf;
+      s1[1] = static_cast<unsigned>(tb + 1) < span ? s1[1] * scale_log2 : kNegInf;
+      s1[2] = static_cast<unsigned>(tb) < span ? s1[2] * scale_log2 : kNegInf;
+      s1[3] = static_cast<unsigned>(tb + 1) < span ? s1[3] * scale_log2 : kNegInf;
       float mx_lo = fmaxf(fmaxf(s0[0], s0[1]), fmaxf(s1[0], s1[1]));
       float mx_hi = fmaxf(fmaxf(s0[2], s0[3]), fmaxf(s1[2], s1[3]));
       mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
@@ -391,8 +400,10 @@ struct CcConsumerF8 {
   }
 
   // Process this warp's 16 tokens (rows cw*16 .. cw*16+15) of one stage;
-  // rows >= nval are past the sequence end and are never used.
-  __device__ __forceinline__ void tile(const uint8_t* stage, int nval, float scale_log2) {
+  // rows >= nval are past the sequence end and rows < nskip before a sliding
+  // window: neither is used.
+  __device__ __forceinline__ void tile(const uint8_t* stage, int nskip, int nval, float scale_log2) {
+    const unsigned span = static_cast<unsigned>(nval - nskip);  // nskip < nval
     const uint8_t* ks = stage;
     const uint8_t* vs = stage + kF8TileBytes;
     float s[8][G];
@@ -414,8 +425,9 @@ struct CcConsumerF8 {
 #pragma unroll
         for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
       }
+      const bool live = static_cast<unsigned>(r - nskip) < span;
 #pragma unroll
-      for (int g = 0; g < G; ++g) s[i][g] = (r < nval) ? part[g] * scale_log2 : kNegInf;
+      for (int g = 0; g < G; ++g) s[i][g] = live ? part[g] * scale_log2 : kNegInf;
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -433,7 +445,7 @@ struct CcConsumerF8 {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = cw * 16 + 2 * i + half;
-      if (r < nval) {
+      if (static_cast<unsigned>(r - nskip) < span) {
         float v[8];
         load8(vs, r, v);
 #pragma unroll
@@ -538,7 +550,8 @@ struct MmaConsumerF8 {
     l[0] = l[1] = 0.f;
   }
 
-  __device__ __forceinline__ void tile(uint8_t* stage, int nval, float scale_log2) {
+  __device__ __forceinline__ void tile(uint8_t* stage, int nskip, int nval, float scale_log2) {
+    const unsigned span = static_cast<unsigned>(nval - nskip);  // nskip < nval
     const uint32_t ks_base = smem_u32(stage);
     const uint32_t vs_base = ks_base + kF8TileBytes;
     const int q4 = lane & 3;
@@ -546,12 +559,16 @@ struct MmaConsumerF8 {
     for (int c = 0; c < kTokensPerWarp / 16; ++c) {
       const int r0 = tok0 + 16 * c;
       if (r0 >= nval) break;
-      if (r0 + 16 > nval) {
-        // Rows past the sequence end may hold anything (even NaN codes); zero
-        // the V rows so that P = 0 there contributes exactly nothing.
+      if (r0 + 16 <= nskip) continue;  // wholly before a sliding window
+      if (r0 + 16 > nval || r0 < nskip) {
+        // Rows past the sequence end (or before a sliding window) may hold
+        // anything, even NaN codes; zero their V rows so that P = 0 there
+        // contributes exactly nothing.  Both ranges are under 16 rows.
         uint8_t* vs = stage + kF8TileBytes;
-        for (int idx = lane; idx < (r0 + 16 - nval) * 8; idx += 32) {
-          const int r = nval + (idx >> 3);
+        const int lo = max(0, nskip - r0), hi = max(0, r0 + 16 - nval);
+        for (int idx = lane; idx < (lo + hi) * 8; idx += 32) {
+          const int k = idx >> 3;
+          const int r = k < lo ? r0 + k : nval + (k - lo);
           *reinterpret_cast<uint4*>(vs + f8_off(r, idx & 7)) = make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
@@ -577,16 +594,17 @@ struct MmaConsumerF8 {
           mma_16816<false>(s1, qa[2 * w + 1], b2, b3);
         }
       }
-      // Scale into the log2 domain and mask tokens past the end.
-      const int ta = r0 + 2 * q4, tb = r0 + 8 + 2 * q4;
-      s0[0] = ta < nval ? s0[0] * scale_log2 : kNegInf;
-      s0[1] = ta + 1 < nval ? s0[1] * scale_log2 : kNegInf;
-      s0[2] = ta < nval ? s0[2] * scale_log2 : kNegInf;
-      s0[3] = ta + 1 < nval ? s0[3] * scale_log2 : kNegInf;
-      s1[0] = tb < nval ? s1[0] * scale_log2 : kNegInf;
-      s1[1] = tb + 1 < nval ? s1[1] * scale_log2 : kNegInf;
-      s1[2] = tb < nval ? s1[2] * scale_log2 : kNegInf;
-      s1[3] = tb + 1 < nval ? s1[3] * scale_log2 : kNegInf;
+      // Scale into the log2 domain and mask tokens outside [nskip, nval).
+      // ta, tb count from the window start: valid rows are [0, span).
+      const int ta = r0 - nskip + 2 * q4, tb = ta + 8;
+      s0[0] = static_cast<unsigned>(ta) < span ? s0[0] * scale_log2 : kNegInf;
+      s0[1] = static_cast<unsigned>(ta + 1) < span ? s0[1] * scale_log2 : kNegInf;
+      s0[2] = static_cast<unsigned>(ta) < span ? s0[2] * scale_log2 : kNegInf;
+      s0[3] = static_cast<unsigned>(ta + 1) < span ? s0[3] * scale_log2 : kNegInf;
+      s1[0] = static_cast<unsigned>(tb) < span ? s1[0] * scale_log2 : kNegInf;
+      s1[1] = static_cast<unsigned>(tb + 1) < span ? s1[1] * scale_log2 : kNegInf;
+      s1[2] = static_cast<unsigned>(tb) < span ? s1[2] * scale_log2 : kNegInf;
+      s1[3] = static_cast<unsigned>(tb + 1) < span ? s1[3] * scale_log2 : kNegInf;
       float mx_lo = fmaxf(fmaxf(s0[0], s0[1]), fmaxf(s1[0], s1[1]));
       float mx_hi = fmaxf(fmaxf(s0[2], s0[3]), fmaxf(s1[2], s1[3]));
       mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
@@ -715,7 +733,13 @@ __global__ void __launch_bounds__(32 * (1 + Consumer::kWarps), Consumer::kMinBlo
     bad = 1;
     if (threadIdx.x == 0 && split == 0 && j == 0) flag_error(p.err_flag, kFlagBadSeqLen);
   }
-  const int t_begin = split * p.tokens_per_split;
+  // A sliding window attends to tokens [w0, seq_len) ("07 · MHA/MQA/GQA/MLA
+  // quick learn": each token attends only to the last W tokens).  Tiles start
+  // at the block (or 64-token) boundary holding w0; blocks wholly before the
+  // window are never read.
+  const int w0 = (p.window > 0 && seq_len > p.window) ? seq_len - p.window : 0;
+  const int base = w0 & ~((p.block_size < kTile ? p.block_size : kTile) - 1);
+  const int t_begin = base + split * p.tokens_per_split;
   const int t_end = bad ? t_begin : min(seq_len, t_begin + p.tokens_per_split);
   if (!bad && t_end > t_begin) {
     const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
@@ -835,8 +859,9 @@ __global__ void __launch_bounds__(32 * (1 + Consumer::kWarps), Consumer::kMinBlo
       ok = false;
       break;
     }
-    const int nval = min(kTile, t_end - (t_begin + it * kTile));
-    c.tile(smem + s * kStage, nval, scale_log2);
+    const int t0 = t_begin + it * kTile;
+    const int nval = min(kTile, t_end - t0);
+    c.tile(smem + s * kStage, max(0, w0 - t0), nval, scale_log2);
     fence_proxy_async_smem();  // order any generic smem writes before the next TMA fill
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);

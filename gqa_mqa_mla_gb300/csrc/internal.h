@@ -32,6 +32,7 @@ struct GqaParams {
   int block_size, log2_block_size, num_blocks, max_blocks_per_seq, max_seq_len;
   int n_split, tokens_per_split;  // tokens_per_split is a multiple of kTile
   float scale_log2;               // scale * log2(e)
+  int window;                     // > 0: attend only to the last `window` tokens
   const float* k_scale;           // [h_kv], 8-bit caches only: K value = e4m3 * k_scale[j]
   const float* v_scale;           // [h_kv], 8-bit caches only
 };

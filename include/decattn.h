@@ -170,6 +170,32 @@ int gqa_decode_fp8kv(const void* q, const void* k_cache, const void* v_cache,
                      float scale, const decattn_launch* launch);
 
 /*
+ * gqa_decode_window, gqa_decode_fp8kv_window -- the same decode restricted to
+ * a sliding window: each sequence's query attends only to its last `window`
+ * tokens ("07 · MHA/MQA/GQA/MLA quick learn", the question on what sliding-
+ * window attention does differently).  For a sequence of length L the
+ * attended tokens are positions [max(0, L - window), L), the newest (the
+ * query's own, already in the cache) included; window >= L is full attention.
+ *   window       >= 1 (else DECATTN_ERR_INVALID_ARG)
+ * Every other argument, layout, status and the workspace rule as gqa_decode
+ * (resp. gqa_decode_fp8kv).  Cache blocks wholly before the window are never
+ * read and their block_table entries are neither read nor checked, so an
+ * engine may have recycled them; the block holding the window's first token
+ * is read whole, but its tokens before the window are not used (their values
+ * may be anything).  Work and the planner's split count scale with
+ * min(max_seq_len, window + min(block_size, 64) - 1), not max_seq_len.
+ */
+int gqa_decode_window(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* seq_lens, void* out, int h_q,
+                      int h_kv, int d_head, float scale, int window,
+                      const decattn_launch* launch);
+int gqa_decode_fp8kv_window(const void* q, const void* k_cache, const void* v_cache,
+                            const float* k_scale, const float* v_scale,
+                            const int32_t* block_table, const int32_t* seq_lens, void* out,
+                            int h_q, int h_kv, int d_head, float scale, int window,
+                            const decattn_launch* launch);
+
+/*
  * mla_decode -- absorbed multi-head latent attention decode ("MQA, GQA, and
  * MLA", section 5; "Why GQA's KV Cache Savings Don't Fully Reduce TPOT",
  * "What Makes MLA Different").  128 heads, d_c = 512, d_rope = 64.
@@ -202,6 +228,10 @@ int gqa_decode_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq
 int gqa_decode_fp8kv_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,
                                  int num_sms);
 int mla_decode_plan_splits(int batch, int max_seq_len, int num_sms);
+/* The windowed calls' planner: kv_bytes = 2 for gqa_decode_window, 1 for
+ * gqa_decode_fp8kv_window; block_size a power of two. */
+int gqa_decode_window_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,
+                                  int window, int block_size, int kv_bytes, int num_sms);
 
 /* Workspace bytes needed for num_splits (>= 1): fp32 partial outputs and
  * log-sum-exps (GQA: one per split per row; MLA: two per share, plus a

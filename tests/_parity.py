@@ -42,6 +42,27 @@ def oracle_gqa_fp8(x: synth.GQAFp8Inputs, rows=None, scale=None):
                                    rows=rows)
 
 
+def oracle_gqa_window(x: synth.GQAInputs, window: int, rows=None, block_table=None,
+                      k_cache=None, v_cache=None):
+    bt = x.block_table if block_table is None else block_table
+    return oracle.gqa_decode_window(synth.u16(x.q), synth.u16(x.k_cache if k_cache is None else k_cache),
+                                    synth.u16(x.v_cache if v_cache is None else v_cache),
+                                    bt.cpu().numpy(), x.seq_lens.cpu().numpy(), dtype=x.dtype,
+                                    scale=x.scale, window=window, rows=rows)
+
+
+def oracle_gqa_fp8_window(x: synth.GQAFp8Inputs, window: int, rows=None, block_table=None,
+                          k_codes=None, v_codes=None):
+    bt = x.block_table if block_table is None else block_table
+    kc = x.k_codes if k_codes is None else k_codes
+    vc = x.v_codes if v_codes is None else v_codes
+    return oracle.gqa_decode_fp8kv_window(synth.u16(x.q), kc.cpu().numpy(), vc.cpu().numpy(),
+                                          x.k_scale.cpu().double().numpy(),
+                                          x.v_scale.cpu().double().numpy(), bt.cpu().numpy(),
+                                          x.seq_lens.cpu().numpy(), q_dtype=x.dtype,
+                                          scale=x.scale, window=window, rows=rows)
+
+
 def oracle_mla(x: synth.MLAInputs, rows=None):
     return oracle.mla_decode(synth.u16(x.q_abs), synth.u16(x.q_rope), synth.u16(x.cache),
                              x.block_table.cpu().numpy(), x.seq_lens.cpu().numpy(), dtype=x.dtype,

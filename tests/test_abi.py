@@ -147,3 +147,42 @@ def test_mla_host_checks(lib, case, expect):
     L = case.pop("L", {})
     L = None if L is None else _launch(**L)
     assert _mla(lib, L, **case) == expect
+
+
+def _gqa_window(lib, L, window, fp8=False):
+    if fp8:
+        return lib.gqa_decode_fp8kv_window(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 2, 128,
+                                           0.088, window, ctypes.byref(L))
+    return lib.gqa_decode_window(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 2, 128, 0.088, window,
+                                 ctypes.byref(L))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_window_host_checks(lib, fp8):
+    for w in (0, -1, -(2**31)):
+        assert _gqa_window(lib, _launch(), w, fp8) == binding.DECATTN_ERR_INVALID_ARG
+    # the shared checks still come first for a valid window
+    assert _gqa_window(lib, _launch(batch=0), 5, fp8) == binding.DECATTN_ERR_INVALID_ARG
+    assert _gqa_window(lib, _launch(dtype=7), 5, fp8) == binding.DECATTN_ERR_INVALID_ARG
+    # a window long enough for 4 splits still needs the workspace for them
+    assert _gqa_window(lib, _launch(num_splits=4), 300, fp8) == binding.DECATTN_ERR_WORKSPACE
+
+
+def test_window_planner_plans_for_the_window_not_the_sequence(lib):
+    for B, h_q, h_kv, S, W, bs in [(1, 64, 8, 131072, 4096, 16), (4, 32, 8, 65536, 1024, 128),
+                                   (2, 8, 1, 8192, 1, 16), (64, 64, 8, 8192, 4096, 16),
+                                   (3, 16, 2, 100, 4096, 16)]:
+        span = min(S, W + min(bs, 64) - 1)
+        for kv_bytes, plan in ((2, binding.gqa_plan_splits), (1, binding.gqa_fp8_plan_splits)):
+            got = binding.gqa_window_plan_splits(B, h_q, h_kv, S, W, bs, kv_bytes, num_sms=152)
+            assert got == plan(B, h_q, h_kv, span, num_sms=152)
+    # a 4k window over a 128k sequence is planned like a 4k sequence, not like 128k
+    assert binding.gqa_window_plan_splits(1, 64, 8, 131072, 4096, 16, num_sms=152) < \
+        binding.gqa_plan_splits(1, 64, 8, 131072, num_sms=152)
+    for bad in [dict(window=0), dict(block_size=24), dict(kv_bytes=4)]:
+        a = dict(batch=2, h_q=8, h_kv=2, max_seq_len=100, window=10, block_size=16, kv_bytes=2)
+        a.update(bad)
+        with pytest.raises(binding.DecAttnError):
+            binding.gqa_window_plan_splits(a["batch"], a["h_q"], a["h_kv"], a["max_seq_len"],
+                                           a["window"], a["block_size"], a["kv_bytes"],
+                                           num_sms=152)
