@@ -484,7 +484,9 @@ def main():
         extras = {"gqa_fp8": {"workload": GQA_FP8_WORKLOAD, "GBps": f_gbps, "ms": f_ms,
                               "steps_per_s": 1e3 / f_ms, "bytes": fb, "steps": nf,
                               "frac_of_hbm_peak": f_gbps / hbm, "splits": f_ns,
-                              "cache_dtype": "e4m3 (per-KV-head fp32 scales)"}}
+                              "cache_dtype": "e4m3 (per-KV-head fp32 scales)",
+                              "traffic": load_traffic("gqa_partial_fp8_llama3_70b",
+                                                      GQA_KERNEL_SOURCES)}}
         err |= int(flag.item())
         del fx, f_ws, f_out
 
@@ -507,7 +509,9 @@ def main():
         extras["gqa_window"] = {"workload": f"{GQA_WORKLOAD} window {GQA_WINDOW}",
                                 "GBps": w_gbps, "ms": w_ms, "steps_per_s": 1e3 / w_ms,
                                 "bytes": wb, "steps": nf, "frac_of_hbm_peak": w_gbps / hbm,
-                                "splits": w_ns}
+                                "splits": w_ns,
+                                "traffic": load_traffic("gqa_partial_window_llama3_70b",
+                                                        GQA_KERNEL_SOURCES)}
         err |= int(flag.item())
         del w_ws, w_out
 
