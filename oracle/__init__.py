@@ -60,6 +60,12 @@ def _load():
             lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_to_double.restype = D
             lib.oracle_dequant_e4m3.argtypes = [P, I64, I, I, P, P]
+            lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+            lib.oracle_e4m3_from_float_array.argtypes = [P, I64, P]
+            lib.oracle_e4m3_from_float_array.restype = None
+            lib.oracle_quant_e4m3.argtypes = [P, I, I64, I, I, P, P]
+            lib.oracle_quant_e4m3.restype = None
             lib.oracle_decode_array.restype = None
             lib.oracle_cache_row.argtypes = [P, I, I, I, I, I]
             lib.oracle_cache_row.restype = I64
@@ -147,6 +153,53 @@ def gqa_decode_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_len
     return gqa_decode(q64, dequant_e4m3(k_codes, k_scale), dequant_e4m3(v_codes, v_scale),
                       block_table, seq_lens, dtype="f64", scale=scale, rows=rows,
                       t_begin=t_begin, t_end=t_end)
+
+
+def e4m3_from_float32(y) -> np.ndarray:
+    """e4m3 codes of float32 values: nearest finite value, ties to the even
+    code, saturating at +-448, sign kept (oracle_e4m3_from_float)."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    out = np.empty(y.shape, dtype=np.uint8)
+    _load().oracle_e4m3_from_float_array(_ptr(y), y.size, _ptr(out))
+    return out
+
+
+def quant_e4m3(x_bits, dtype: str, scales) -> np.ndarray:
+    """Quantise 16-bit values [..., h_kv, d] (raw bits) to e4m3 codes with one
+    fp32 scale per KV head: code = e4m3(fp32(x) / scale[j])."""
+    x = _elems(x_bits, dtype)
+    s = np.ascontiguousarray(scales, dtype=np.float32)
+    h_kv, d = x.shape[-2], x.shape[-1]
+    assert s.shape == (h_kv,)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_quant_e4m3(_ptr(x), _DTYPES[dtype], x.size // (h_kv * d), h_kv, d, _ptr(s),
+                              _ptr(out))
+    return out
+
+
+def kv_append(cache, new_rows, positions, block_table):
+    """Decode-step append: sequence b's new token row (new_rows[b], any shape
+    matching one cache slot) is written to slot positions[b] % block_size of
+    block block_table[b][positions[b] // block_size] of a copy of `cache`
+    [num_blocks, block_size, ...].  A negative position skips the sequence; a
+    position past the table or a block id outside [0, num_blocks) skips it
+    and is reported.  Returns (new cache, {b: "bad_position" | "bad_block"})."""
+    out = np.array(cache, copy=True)
+    nb, bs = out.shape[0], out.shape[1]
+    bt = np.asarray(block_table, dtype=np.int32)
+    bad = {}
+    for b, pos in enumerate(np.asarray(positions, dtype=np.int64).tolist()):
+        if pos < 0:
+            continue
+        if pos // bs >= bt.shape[1]:
+            bad[b] = "bad_position"
+            continue
+        blk = int(bt[b, pos // bs])
+        if blk < 0 or blk >= nb:
+            bad[b] = "bad_block"
+            continue
+        out[blk, pos % bs] = new_rows[b]
+    return out, bad
 
 
 def cache_row(block_table: np.ndarray, block_size: int, num_blocks: int, b: int, t: int) -> int:

@@ -114,6 +114,48 @@ void oracle_dequant_e4m3(const uint8_t* codes, int64_t rows, int h_kv, int d,
       }
 }
 
+/* e4m3 code of the finite e4m3 value nearest to y (largest magnitude 448):
+ * ties go to the even code (last fraction bit 0); every magnitude above 448,
+ * infinity included, takes 448 (saturation); the sign is kept, zero
+ * included; NaN gives the NaN code 0x7F.  Written as a search over the 127
+ * non-negative finite codes, so that it is checkable by eye. */
+uint8_t oracle_e4m3_from_float(float y) {
+  if (isnan(y)) return 0x7F;
+  const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+  if (isinf(y)) return sign | 0x7E;
+  const double a = fabs((double)y);
+  int best = 0;
+  double best_d = a; /* distance to code 0x00 (value 0) */
+  for (int c = 1; c <= 0x7E; ++c) {
+    const double d = fabs(oracle_e4m3_to_double((uint8_t)c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+void oracle_e4m3_from_float_array(const float* y, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_from_float(y[i]);
+}
+
+/* Quantise 16-bit values laid out [rows][h_kv][d] to e4m3 codes with one
+ * scale per KV head: code = e4m3 nearest to (fp32 x) / scale[j], the
+ * quotient rounded to fp32 (the cached value is then e4m3(code) * scale[j]). */
+void oracle_quant_e4m3(const uint16_t* x, int dtype, int64_t rows, int h_kv, int d,
+                       const float* scale, uint8_t* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int j = 0; j < h_kv; ++j)
+      for (int e = 0; e < d; ++e) {
+        const int64_t i = (r * h_kv + j) * d + e;
+        const float xf = (float)(dtype == ORACLE_FP16 ? oracle_half_to_double(x[i])
+                                                      : oracle_bf16_to_double(x[i]));
+        const float q = xf / scale[j];
+        out[i] = oracle_e4m3_from_float(q);
+      }
+}
+
 void oracle_decode_array(const uint16_t* src, int dtype, int64_t n, double* dst) {
   for (int64_t i = 0; i < n; ++i)
     dst[i] = dtype == ORACLE_FP16 ? oracle_half_to_double(src[i]) : oracle_bf16_to_double(src[i]);

@@ -608,3 +608,93 @@ def test_fp8kv_window_reduces_to_the_full_fp8_path_and_to_one_value():
             j = i // 2
             expect = oracle.e4m3_to_double(codes_v[bt[b, t // bs], t % bs, j]) * vs[j]
             assert np.array_equal(one[b * h_q + i], expect)
+
+
+# ---------------------------------------------------------------- e4m3 encoding and KV append
+
+def test_e4m3_encoding_round_trips_every_finite_code():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    values = oracle.e4m3_to_double(codes).astype(np.float32)  # exact in fp32
+    assert np.array_equal(oracle.e4m3_from_float32(values), codes)  # -0 keeps its sign too
+
+
+def test_e4m3_encoding_matches_torch_rounding_inside_the_range():
+    """torch's float8_e4m3fn cast rounds to nearest even; inside +-448 it must agree."""
+    g = torch.Generator().manual_seed(17)
+    y = torch.cat([torch.randn(200000, generator=g) * s for s in (0.01, 1.0, 30.0, 150.0)])
+    y = y.clamp(-448, 448)
+    ref = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_from_float32(y.numpy())
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_encoding_ties_saturation_and_specials():
+    f = lambda v: int(oracle.e4m3_from_float32([v])[0])
+    # ties go to the even code: between 2^-6 (0x08) and 1.125 * 2^-6 (0x09) -> 0x08,
+    # between 0x09 and 0x0A (1.25 * 2^-6) -> 0x0A
+    assert f(2.0**-6 * 1.0625) == 0x08
+    assert f(2.0**-6 * 1.1875) == 0x0A
+    assert f(2.0**-6 * 1.0625 * (1 + 2**-20)) == 0x09  # just above the tie
+    # below half the smallest subnormal (2^-9) is zero; the half itself ties to 0x00
+    assert f(2.0**-10) == 0x00 and f(2.0**-10 * 1.001) == 0x01 and f(-(2.0**-11)) == 0x80
+    # saturation at 448 in place of overflow; infinities saturate; NaN stays NaN
+    assert f(449.0) == 0x7E and f(464.0) == 0x7E and f(1e30) == 0x7E and f(-1e30) == 0xFE
+    assert f(float("inf")) == 0x7E and f(float("-inf")) == 0xFE and f(float("nan")) == 0x7F
+    # largest step: 416 (0x7D) .. 448 (0x7E); 432 is the tie -> even code 0x7E
+    assert f(430.0) == 0x7D and f(432.0) == 0x7E and f(433.0) == 0x7E
+
+
+def test_quantisation_divides_by_each_kv_heads_scale():
+    rng = np.random.default_rng(31)
+    codes = rng.integers(0, 0x7E, (3, 2, 16), dtype=np.uint8)  # positive finite codes
+    scale = np.array([0.5, 0.03125], dtype=np.float32)  # powers of two: products exact
+    vals = oracle.e4m3_to_double(codes) * scale[None, :, None]
+    bits = torch.from_numpy(vals.astype(np.float32)).to(torch.bfloat16).view(torch.int16)
+    bits = bits.numpy().view(np.uint16)
+    back = oracle.bf16_to_double(bits)
+    assert np.array_equal(back, vals)  # every value is exact in bf16
+    assert np.array_equal(oracle.quant_e4m3(bits, "bf16", scale), codes)
+    # swapping the heads' scales moves every code of the two heads
+    wrong = oracle.quant_e4m3(bits, "bf16", scale[::-1].copy())
+    assert np.all(wrong[:, 0][codes[:, 0] > 0x10] != codes[:, 0][codes[:, 0] > 0x10])
+
+
+def test_kv_append_writes_exactly_one_slot_per_sequence():
+    rng = np.random.default_rng(32)
+    nb, bs, h_kv, d = 9, 4, 2, 8
+    cache = rng.standard_normal((nb, bs, h_kv, d))
+    bt = np.array([[3, 7, -1], [0, 5, 8], [1, 2, 4], [6, -1, -1]], np.int32)
+    new = rng.standard_normal((4, h_kv, d))
+    pos = np.array([5, 8, -1, 4], np.int64)  # seq 1 starts block 2; seq 2 skips; seq 3 has no block
+    out, bad = oracle.kv_append(cache, new, pos, bt)
+    assert bad == {3: "bad_block"}
+    assert np.array_equal(out[7, 1], new[0])      # position 5 = block 1 (id 7), slot 1
+    assert np.array_equal(out[8, 0], new[1])      # position 8 = block 2 (id 8), slot 0
+    changed = np.any(out != cache, axis=(2, 3))
+    assert changed.sum() == 2 and changed[7, 1] and changed[8, 0]
+    _, bad = oracle.kv_append(cache, new, np.array([12, -5, -5, -5]), bt)
+    assert bad == {0: "bad_position"}              # past the table's 3 blocks
+    # read back through the decode path's gather: token 5 of sequence 0 is the new row
+    row = oracle.cache_row(bt, bs, nb, 0, 5)
+    assert np.array_equal(out.reshape(nb * bs, h_kv, d)[row], new[0])
+
+
+def test_appending_then_attending_equals_attending_over_the_longer_sequence():
+    """Append the next token then decode over L + 1 tokens = decode over a
+    contiguous copy of the L + 1 tokens."""
+    rng = np.random.default_rng(33)
+    bs, h_kv, d, h_q, L = 4, 2, 8, 4, 10
+    nb = 5
+    k = rng.standard_normal((nb, bs, h_kv, d))
+    v = rng.standard_normal((nb, bs, h_kv, d))
+    bt = np.array([[4, 0, 2]], np.int32)
+    kn, vn = rng.standard_normal((1, h_kv, d)), rng.standard_normal((1, h_kv, d))
+    k2, _ = oracle.kv_append(k, kn, [L], bt)
+    v2, _ = oracle.kv_append(v, vn, [L], bt)
+    q = rng.standard_normal((1, h_q, d))
+    o, l = _gqa(q, k2, v2, bt, np.array([L + 1], np.int32), 0.3)
+    seq_k = np.stack([k[bt[0, t // bs], t % bs] for t in range(L)] + [kn[0]])[None]
+    seq_v = np.stack([v[bt[0, t // bs], t % bs] for t in range(L)] + [vn[0]])[None]
+    o_ref, l_ref = _gqa(q, seq_k, seq_v, np.zeros((1, 1), np.int32), np.array([L + 1], np.int32),
+                        0.3)
+    assert np.array_equal(o, o_ref) and np.array_equal(l, l_ref)
