@@ -515,6 +515,43 @@ def main():
         err |= int(flag.item())
         del w_ws, w_out
 
+        # The decode step's cache write for the same layer: each sequence's new
+        # K and V rows into their paged slot.  The rows written are the ones
+        # already at each sequence's last position, so the cache (and the
+        # CPU baseline's parity check that follows) stays bit for bit as drawn.
+        a_pos = (gx.seq_lens - 1).clamp(min=0).to(torch.int32)
+        a_rows = (gx.block_table[torch.arange(gx.batch, device=dev), a_pos.long() // gx.block_size]
+                  .long() * gx.block_size + a_pos.long() % gx.block_size)
+        a_k = gx.k_cache.view(-1, gx.h_kv, gx.d_head)[a_rows].contiguous()
+        a_v = gx.v_cache.view(-1, gx.h_kv, gx.d_head)[a_rows].contiguous()
+
+        def a_call():
+            da.gqa_kv_append(a_k, a_v, a_pos, gx.block_table, gx.k_cache, gx.v_cache,
+                             err_flag=flag)
+
+        a_ms = time_calls(a_call, nf, stream, dev)
+        # The same calls captured in a CUDA graph and replayed: the device-side
+        # cost without the Python binding's per-call overhead.
+        a_graph = torch.cuda.CUDAGraph()
+        a_side = torch.cuda.Stream(dev)
+        a_side.wait_stream(stream)
+        with torch.cuda.stream(a_side):
+            a_call()  # warm the path on the capture stream
+            with torch.cuda.graph(a_graph, stream=a_side):
+                for _ in range(20):
+                    a_call()
+        stream.wait_stream(a_side)
+        ag_ms = time_calls(a_graph.replay, max(3, nf // 20), stream, dev) / 20
+        a_bytes = 2 * 2 * int((a_pos >= 0).sum().item()) * gx.h_kv * gx.d_head * 2
+        extras["kv_append"] = {"workload": f"{GQA_WORKLOAD} new-token K/V write",
+                               "us_per_call": a_ms * 1e3, "us_per_call_graph": ag_ms * 1e3,
+                               "bytes": a_bytes, "steps": nf,
+                               "GBps_graph": a_bytes / (ag_ms * 1e-3) / 1e9,
+                               "note": "launch-bound (0.5 MB per call); us_per_call includes "
+                                       "the Python binding, the graph figure is device time"}
+        err |= int(flag.item())
+        del a_graph
+
     parts_out = {}
     for name, ms in part_ms.items():
         gbps = part_bytes[name] / (ms * 1e-3) / 1e9

@@ -2,8 +2,9 @@
 
 MHA / GQA / MQA (``gqa_decode``, ``gqa_decode_fp8kv`` over an 8-bit e4m3 KV
 cache, and their sliding-window forms ``gqa_decode_window`` /
-``gqa_decode_fp8kv_window``) and absorbed MLA (``mla_decode``), hand-written
-CUDA kernels for sm_103a behind a C ABI (include/decattn.h).  This package is
+``gqa_decode_fp8kv_window``) and absorbed MLA (``mla_decode``), plus the decode
+step's cache write (``gqa_kv_append``, ``gqa_kv_append_fp8kv``,
+``mla_kv_append``); hand-written CUDA kernels for sm_103a behind a C ABI (include/decattn.h).  This package is
 the thin Python binding; ``synth`` draws seeded synthetic inputs.
 """
 from .binding import (  # noqa: F401
@@ -16,6 +17,8 @@ from .binding import (  # noqa: F401
     gqa_decode_fp8kv_window,
     gqa_decode_window,
     gqa_fp8_plan_splits,
+    gqa_kv_append,
+    gqa_kv_append_fp8kv,
     gqa_plan_splits,
     gqa_window_plan_splits,
     gqa_workspace_size,
@@ -24,6 +27,7 @@ from .binding import (  # noqa: F401
     library_path,
     mla_bytes_per_token,
     mla_decode,
+    mla_kv_append,
     mla_plan_splits,
     mla_workspace_size,
     status_string,

@@ -85,6 +85,12 @@ def lib() -> ctypes.CDLL:
             L.gqa_decode_fp8kv_window.restype = I
             L.gqa_decode_window_plan_splits.argtypes = [I, I, I, I, I, I, I, I, I]
             L.gqa_decode_window_plan_splits.restype = I
+            L.gqa_kv_append.argtypes = [P, P, P, P, P, P, I, I, LP]
+            L.gqa_kv_append.restype = I
+            L.gqa_kv_append_fp8kv.argtypes = [P, P, P, P, P, P, P, P, I, I, LP]
+            L.gqa_kv_append_fp8kv.restype = I
+            L.mla_kv_append.argtypes = [P, P, P, P, LP]
+            L.mla_kv_append.restype = I
             L.mla_decode.argtypes = [P, P, P, P, P, P, F, LP]
             L.mla_decode.restype = I
             L.gqa_decode_plan_splits.argtypes = [I, I, I, I, I, I]
@@ -307,6 +313,89 @@ def gqa_decode_fp8kv_window(q, k_codes, v_codes, k_scale, v_scale, block_table, 
     """gqa_decode_fp8kv restricted to each sequence's last `window` tokens."""
     return gqa_decode_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens,
                             window=window, **kw)
+
+
+def _append_launch(new, cache, block_table, dtype, err_flag, stream) -> Launch:
+    return make_launch(new.shape[0], cache.shape[0], cache.shape[1], block_table.shape[1], 0, 1,
+                       _DT[dtype], None, 0, _ptr(err_flag), _stream_handle(stream))
+
+
+def gqa_kv_append(k_new, v_new, positions, block_table, k_cache, v_cache, *, err_flag=None,
+                  stream=None):
+    """Write each sequence's new K/V rows [B, h_kv, d] into slot positions[b]
+    of its paged 16-bit cache (in place); a negative position skips."""
+    _check(k_new, "k_new", ndim=3)
+    _check(v_new, "v_new", k_new.dtype, 3)
+    _check(k_cache, "k_cache", k_new.dtype, 4)
+    _check(v_cache, "v_cache", k_new.dtype, 4)
+    _check(positions, "positions", torch.int32, 1)
+    _check(block_table, "block_table", torch.int32, 2)
+    if k_new.dtype not in _DT:
+        raise TypeError("k_new must be float16 or bfloat16")
+    B, h_kv, d = k_new.shape
+    if v_new.shape != k_new.shape or k_cache.shape[2:] != (h_kv, d) or \
+            v_cache.shape != k_cache.shape or positions.shape != (B,) or block_table.shape[0] != B:
+        raise ValueError("kv_append: shape mismatch")
+    L = _append_launch(k_new, k_cache, block_table, k_new.dtype, err_flag, stream)
+    st = lib().gqa_kv_append(k_new.data_ptr(), v_new.data_ptr(), positions.data_ptr(),
+                             block_table.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), h_kv,
+                             d, ctypes.byref(L))
+    if st != DECATTN_OK:
+        raise DecAttnError("gqa_kv_append", st)
+
+
+def gqa_kv_append_fp8kv(k_new, v_new, k_scale, v_scale, positions, block_table, k_codes, v_codes,
+                        *, err_flag=None, stream=None):
+    """Quantise each sequence's new K/V rows [B, h_kv, d] (fp16/bf16) to e4m3
+    codes with the per-KV-head scales and write them into slot positions[b]
+    of the 8-bit cache (uint8 or float8_e4m3fn, in place)."""
+    if k_codes.dtype == torch.float8_e4m3fn:
+        k_codes = k_codes.view(torch.uint8)
+    if v_codes.dtype == torch.float8_e4m3fn:
+        v_codes = v_codes.view(torch.uint8)
+    _check(k_new, "k_new", ndim=3)
+    _check(v_new, "v_new", k_new.dtype, 3)
+    _check(k_scale, "k_scale", torch.float32, 1)
+    _check(v_scale, "v_scale", torch.float32, 1)
+    _check(k_codes, "k_codes", torch.uint8, 4)
+    _check(v_codes, "v_codes", torch.uint8, 4)
+    _check(positions, "positions", torch.int32, 1)
+    _check(block_table, "block_table", torch.int32, 2)
+    if k_new.dtype not in _DT:
+        raise TypeError("k_new must be float16 or bfloat16")
+    B, h_kv, d = k_new.shape
+    if v_new.shape != k_new.shape or k_codes.shape[2:] != (h_kv, d) or \
+            v_codes.shape != k_codes.shape or positions.shape != (B,) or \
+            block_table.shape[0] != B or k_scale.shape != (h_kv,) or v_scale.shape != (h_kv,):
+        raise ValueError("kv_append_fp8kv: shape mismatch")
+    L = _append_launch(k_new, k_codes, block_table, k_new.dtype, err_flag, stream)
+    st = lib().gqa_kv_append_fp8kv(k_new.data_ptr(), v_new.data_ptr(), k_scale.data_ptr(),
+                                   v_scale.data_ptr(), positions.data_ptr(),
+                                   block_table.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
+                                   h_kv, d, ctypes.byref(L))
+    if st != DECATTN_OK:
+        raise DecAttnError("gqa_kv_append_fp8kv", st)
+
+
+def mla_kv_append(latent_new, positions, block_table, latent_cache, *, err_flag=None,
+                  stream=None):
+    """Write each sequence's new latent row [B, 576] (c_t then the RoPE key)
+    into slot positions[b] of the paged latent cache (in place)."""
+    _check(latent_new, "latent_new", ndim=2)
+    _check(latent_cache, "latent_cache", latent_new.dtype, 3)
+    _check(positions, "positions", torch.int32, 1)
+    _check(block_table, "block_table", torch.int32, 2)
+    if latent_new.dtype not in _DT:
+        raise TypeError("latent_new must be float16 or bfloat16")
+    B = latent_new.shape[0]
+    if latent_new.shape[1] != 576 or latent_cache.shape[2] != 576 or positions.shape != (B,) or \
+            block_table.shape[0] != B:
+        raise ValueError("mla_kv_append: shape mismatch")
+    L = _append_launch(latent_new, latent_cache, block_table, latent_new.dtype, err_flag, stream)
+    st = lib().mla_kv_append(latent_new.data_ptr(), positions.data_ptr(), block_table.data_ptr(),
+                             latent_cache.data_ptr(), ctypes.byref(L))
+    if st != DECATTN_OK:
+        raise DecAttnError("mla_kv_append", st)
 
 
 def mla_decode(q_absorbed, q_rope, latent_cache, block_table, seq_lens, *, scale: float,

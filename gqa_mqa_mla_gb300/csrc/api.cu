@@ -453,4 +453,75 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
   return DECATTN_OK;
 }
 
+// The decode step's cache write (gqa_kv_append, gqa_kv_append_fp8kv,
+// mla_kv_append): host checks, then one launch for K and V.
+static int kv_append_impl(const void* k_new, const void* v_new, const float* k_scale,
+                          const float* v_scale, bool e4m3, const int32_t* positions,
+                          const int32_t* block_table, void* k_cache, void* v_cache, int row_elems,
+                          int head_elems, bool mla, const decattn_launch* L) {
+  if (!L) return DECATTN_ERR_INVALID_ARG;
+  if (L->batch < 1 || L->num_blocks < 1 || L->max_blocks_per_seq < 1)
+    return DECATTN_ERR_INVALID_ARG;
+  if (L->dtype != DECATTN_FP16 && L->dtype != DECATTN_BF16) return DECATTN_ERR_INVALID_ARG;
+  if (!is_pow2(L->block_size)) return DECATTN_ERR_INVALID_ARG;
+  if (L->block_size < 8 || L->block_size > (mla ? 64 : 256)) return DECATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(L->num_blocks) * L->block_size > 0x7fffffffLL)
+    return DECATTN_ERR_UNSUPPORTED;
+  if (!k_new || !k_cache || !positions || !block_table) return DECATTN_ERR_INVALID_ARG;
+  if (!mla && (!v_new || !v_cache)) return DECATTN_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(k_cache, 16) || !aligned(positions, 4) ||
+      !aligned(block_table, 4) || (v_new && !aligned(v_new, 16)) ||
+      (v_cache && !aligned(v_cache, 16)))
+    return DECATTN_ERR_INVALID_ARG;
+  if (e4m3 && (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4)))
+    return DECATTN_ERR_INVALID_ARG;
+  if (L->err_flag && !aligned(L->err_flag, 4)) return DECATTN_ERR_INVALID_ARG;
+
+  AppendParams p{};
+  p.k_new = k_new;
+  p.v_new = mla ? nullptr : v_new;
+  p.positions = positions;
+  p.block_table = block_table;
+  p.k_cache = k_cache;
+  p.v_cache = mla ? nullptr : v_cache;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.err_flag = L->err_flag;
+  p.batch = L->batch;
+  p.row_elems = row_elems;
+  p.head_elems = head_elems;
+  p.block_size = L->block_size;
+  p.log2_block_size = ilog2(L->block_size);
+  p.num_blocks = L->num_blocks;
+  p.max_blocks_per_seq = L->max_blocks_per_seq;
+  const cudaError_t e = launch_append(p, e4m3, L->dtype == DECATTN_BF16,
+                                      static_cast<cudaStream_t>(L->stream));
+  return e == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
+}
+
+int gqa_kv_append(const void* k_new, const void* v_new, const int32_t* positions,
+                  const int32_t* block_table, void* k_cache, void* v_cache, int h_kv, int d_head,
+                  const decattn_launch* L) {
+  if (h_kv < 1 || h_kv > 1024) return DECATTN_ERR_INVALID_ARG;
+  if (d_head != kHeadDim) return DECATTN_ERR_UNSUPPORTED;
+  return kv_append_impl(k_new, v_new, nullptr, nullptr, false, positions, block_table, k_cache,
+                        v_cache, h_kv * kHeadDim, kHeadDim, false, L);
+}
+
+int gqa_kv_append_fp8kv(const void* k_new, const void* v_new, const float* k_scale,
+                        const float* v_scale, const int32_t* positions,
+                        const int32_t* block_table, void* k_cache, void* v_cache, int h_kv,
+                        int d_head, const decattn_launch* L) {
+  if (h_kv < 1 || h_kv > 1024) return DECATTN_ERR_INVALID_ARG;
+  if (d_head != kHeadDim) return DECATTN_ERR_UNSUPPORTED;
+  return kv_append_impl(k_new, v_new, k_scale, v_scale, true, positions, block_table, k_cache,
+                        v_cache, h_kv * kHeadDim, kHeadDim, false, L);
+}
+
+int mla_kv_append(const void* latent_new, const int32_t* positions, const int32_t* block_table,
+                  void* latent_cache, const decattn_launch* L) {
+  return kv_append_impl(latent_new, nullptr, nullptr, nullptr, false, positions, block_table,
+                        latent_cache, nullptr, kMlaWidth, kMlaWidth, true, L);
+}
+
 }  // extern "C"

@@ -66,6 +66,21 @@ struct MlaCombineParams {
   int batch, n_pairs;
 };
 
+// Decode-step cache write: one new row per sequence.
+struct AppendParams {
+  const void* k_new;          // [B, row_elems] 16-bit (the MLA latent row for mla)
+  const void* v_new;          // [B, row_elems] 16-bit, or null (MLA: one cache)
+  const int32_t* positions;   // [B] slot index of the new token; < 0 skips
+  const int32_t* block_table; // [B, max_blocks_per_seq]
+  void* k_cache;              // [num_blocks, block_size, row_elems]
+  void* v_cache;
+  const float* k_scale;       // [row_elems / head_elems], 8-bit caches only
+  const float* v_scale;
+  int* err_flag;
+  int batch, row_elems, head_elems;
+  int block_size, log2_block_size, num_blocks, max_blocks_per_seq;
+};
+
 struct CombineParams {
   const float* part_o;
   const float* part_lse;
@@ -88,6 +103,8 @@ cudaError_t launch_mla_partial(const MlaParams& p, const CUtensorMap& tm_qa,
                                const CUtensorMap& tm_c, const CUtensorMap& tm_out,
                                const CUtensorMap& tm_po, bool bf16, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int d, bool bf16, cudaStream_t stream);
+// e4m3: quantise with k_scale / v_scale (bf16 or fp16 input); else a copy.
+cudaError_t launch_append(const AppendParams& p, bool e4m3, bool bf16, cudaStream_t stream);
 cudaError_t launch_mla_combine(const MlaCombineParams& p, bool bf16, cudaStream_t stream);
 
 // Planner shared by the front end and the workspace query.

@@ -266,6 +266,14 @@ DECATTN_DEV void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
       : "r"(w));
 }
 
+// Two floats to two e4m3 codes (round to nearest even, saturating to the
+// largest finite magnitude 448), x in the lower byte.
+DECATTN_DEV uint32_t f32x2_to_e4m3x2(float x, float y) {
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(y), "f"(x));
+  return h;
+}
+
 DECATTN_DEV uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));

@@ -241,6 +241,14 @@ def mla_inputs(batch: int, seq_lens=8192, block_size: int = 64, dtype: str = "bf
                      scale=(1.0 / math.sqrt(128 + 64)) if scale is None else scale)
 
 
+def new_token_rows(batch: int, row_shape, dtype: str = "bf16", seed: int = 0, std: float = 1.0,
+                   device="cpu") -> torch.Tensor:
+    """[batch, *row_shape] rows of one new token per sequence (its K or V
+    heads, or its MLA latent row), N(0, std^2) rounded to the storage dtype."""
+    g = _gen(device, seed + 15485863)
+    return _randn((batch, *row_shape), dtype, std, g, device)
+
+
 def u16(t: torch.Tensor) -> np.ndarray:
     """Raw 16-bit storage of a fp16/bf16 tensor as a host uint16 numpy array."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)

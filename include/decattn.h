@@ -221,6 +221,43 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
                const int32_t* block_table, const int32_t* seq_lens, void* out, float scale,
                const decattn_launch* launch);
 
+/*
+ * gqa_kv_append, gqa_kv_append_fp8kv, mla_kv_append -- the decode step's
+ * cache write: each sequence's new token joins the paged cache before its
+ * query attends ("Compressing the KV Cache: DeepSeek's Latent Projections
+ * (MLA) vs. Meta's Grouped Queries (GQA)": generation keeps the keys and
+ * values of every past token in GPU memory, and "KV-Cache Management
+ * Guardrails" keeps that cache in a paging engine; "MQA, GQA, and MLA",
+ * section 5: MLA caches the latent with the decoupled RoPE key beside it).
+ *   k_new, v_new   [batch, h_kv, d_head] in launch->dtype (fp16 / bf16)
+ *   latent_new     [batch, 576] in launch->dtype: latent c_t then the RoPE key
+ *   positions      [batch] int32: the slot the token takes in its sequence
+ *                  (its position, normally the length before this step); a
+ *                  negative position leaves the sequence untouched
+ *   block_table    [batch, max_blocks_per_seq] int32
+ *   k_cache, v_cache, latent_cache  the paged caches of gqa_decode,
+ *                  gqa_decode_fp8kv and mla_decode; only the addressed slot
+ *                  of each sequence is written
+ *   k_scale, v_scale  [h_kv] fp32 (gqa_kv_append_fp8kv): value x of KV head
+ *                  j is stored as the e4m3 code nearest to fp32(x) / scale[j]
+ *                  (ties to even, magnitudes beyond 448 saturate to 448), so
+ *                  gqa_decode_fp8kv reads back e4m3(code) * scale[j]
+ * Of the launch block only batch, num_blocks, block_size, max_blocks_per_seq,
+ * dtype, err_flag and stream are used (block_size as for the matching decode
+ * call).  A position past the block table sets DECATTN_FLAG_BAD_SEQ_LEN, an
+ * out-of-range block id DECATTN_FLAG_BAD_BLOCK; that sequence is skipped,
+ * the others are written.  Sequences must name distinct slots.
+ */
+int gqa_kv_append(const void* k_new, const void* v_new, const int32_t* positions,
+                  const int32_t* block_table, void* k_cache, void* v_cache, int h_kv, int d_head,
+                  const decattn_launch* launch);
+int gqa_kv_append_fp8kv(const void* k_new, const void* v_new, const float* k_scale,
+                        const float* v_scale, const int32_t* positions,
+                        const int32_t* block_table, void* k_cache, void* v_cache, int h_kv,
+                        int d_head, const decattn_launch* launch);
+int mla_kv_append(const void* latent_new, const int32_t* positions, const int32_t* block_table,
+                  void* latent_cache, const decattn_launch* launch);
+
 /* Split count the automatic planner picks (num_splits = 0).  num_sms <= 0
  * queries the current device.  Returns >= 1, or a negative status. */
 int gqa_decode_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,

@@ -186,3 +186,46 @@ def test_window_planner_plans_for_the_window_not_the_sequence(lib):
             binding.gqa_window_plan_splits(a["batch"], a["h_q"], a["h_kv"], a["max_seq_len"],
                                            a["window"], a["block_size"], a["kv_bytes"],
                                            num_sms=152)
+
+
+def _append(lib, kind, L, **kw):
+    a = dict(k=FAKE, v=FAKE, ks=FAKE, vs=FAKE, pos=FAKE, bt=FAKE, kc=FAKE, vc=FAKE, h_kv=2, d=128)
+    a.update(kw)
+    Lp = None if L is None else ctypes.byref(L)
+    if kind == "gqa":
+        return lib.gqa_kv_append(a["k"], a["v"], a["pos"], a["bt"], a["kc"], a["vc"], a["h_kv"],
+                                 a["d"], Lp)
+    if kind == "fp8":
+        return lib.gqa_kv_append_fp8kv(a["k"], a["v"], a["ks"], a["vs"], a["pos"], a["bt"],
+                                       a["kc"], a["vc"], a["h_kv"], a["d"], Lp)
+    return lib.mla_kv_append(a["k"], a["pos"], a["bt"], a["kc"], Lp)
+
+
+@pytest.mark.parametrize("kind", ["gqa", "fp8", "mla"])
+@pytest.mark.parametrize("case,expect", [
+    (dict(L=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(k=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(pos=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(kc=FAKE + 8), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(pos=FAKE + 2), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(batch=0)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(dtype=3)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(block_size=12)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(block_size=4)), binding.DECATTN_ERR_UNSUPPORTED),
+    (dict(L=dict(err_flag=FAKE + 1)), binding.DECATTN_ERR_INVALID_ARG),
+])
+def test_kv_append_host_checks(lib, kind, case, expect):
+    case = dict(case)
+    L = case.pop("L", {})
+    L = None if L is None else _launch(**L)
+    assert _append(lib, kind, L, **case) == expect
+
+
+def test_kv_append_kind_specific_checks(lib):
+    L = _launch()
+    assert _append(lib, "gqa", L, v=None) == binding.DECATTN_ERR_INVALID_ARG
+    assert _append(lib, "gqa", L, d=64) == binding.DECATTN_ERR_UNSUPPORTED
+    assert _append(lib, "gqa", L, h_kv=0) == binding.DECATTN_ERR_INVALID_ARG
+    assert _append(lib, "fp8", L, ks=None) == binding.DECATTN_ERR_INVALID_ARG
+    assert _append(lib, "fp8", L, vs=FAKE + 2) == binding.DECATTN_ERR_INVALID_ARG
+    assert _append(lib, "mla", _launch(block_size=128)) == binding.DECATTN_ERR_UNSUPPORTED
