@@ -331,6 +331,42 @@ def mla_explicit(q_nope, q_rope, c, k_rope, w_uk, w_uv, *, scale: float):
     return out, scores
 
 
+def mla_absorb_q(q_nope, w_uk, *, dtype: str) -> np.ndarray:
+    """The query-side absorption ("MQA, GQA, and MLA", section 5: q_i . k_i =
+    x (W_q^(i) W_uk^(i)^T) c^T, so the per-head query times W_uk^(i)^T scores
+    directly against the cached latent): q_abs[b, i, :] = q_nope[b, i, :]
+    W_uk^(i)^T in fp64.
+
+    q_nope [B, H, d_h]; w_uk [H, d_c, d_h] with w_uk[i] = W_uk^(i) (k_i = c
+    W_uk^(i)).  Returns [B, H, d_c] float64.
+    """
+    q = _elems(q_nope, dtype)
+    w = _elems(w_uk, dtype)
+    if dtype != "f64":
+        q, w = _to_f64(q, dtype), _to_f64(w, dtype)
+    return np.einsum("bie,ice->bic", q, w)
+
+
+def mla_unabsorb_out(o_lat, w_uv_t, *, dtype: str) -> np.ndarray:
+    """The value-side step after the latent attention: the head's output is
+    its softmax-weighted latent times W_uv^(i) (v_i = c W_uv^(i), so
+    sum_t p_t v_{i,t} = (sum_t p_t c_t) W_uv^(i)): out[b, i, :] =
+    o_lat[b, i, :] W_uv^(i) in fp64.
+
+    o_lat [B, H, d_c]; w_uv_t [H, d_v, d_c] with w_uv_t[i] = W_uv^(i)^T.
+    Returns [B, H, d_v] float64.
+    """
+    o = _elems(o_lat, dtype)
+    w = _elems(w_uv_t, dtype)
+    if dtype != "f64":
+        o, w = _to_f64(o, dtype), _to_f64(w, dtype)
+    return np.einsum("bic,ivc->biv", o, w)
+
+
+def _to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    return half_to_double(bits) if dtype == "fp16" else bf16_to_double(bits)
+
+
 def lse_merge(o_parts, lse_parts):
     """Merge partial (o, lse) over disjoint token ranges. o_parts [n, d], lse_parts [n]."""
     o = np.ascontiguousarray(o_parts, dtype=np.float64)

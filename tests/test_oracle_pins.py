@@ -698,3 +698,64 @@ def test_appending_then_attending_equals_attending_over_the_longer_sequence():
     o_ref, l_ref = _gqa(q, seq_k, seq_v, np.zeros((1, 1), np.int32), np.array([L + 1], np.int32),
                         0.3)
     assert np.array_equal(o, o_ref) and np.array_equal(l, l_ref)
+
+
+# ---------------------------------------------------------------- MLA absorption GEMMs
+
+def test_absorption_gemms_match_brute_force_loops():
+    rng = np.random.default_rng(40)
+    B, H, d_h, d_c, d_v = 2, 3, 4, 5, 6
+    q = rng.standard_normal((B, H, d_h))
+    w_uk = rng.standard_normal((H, d_c, d_h))
+    o = rng.standard_normal((B, H, d_c))
+    w_uv_t = rng.standard_normal((H, d_v, d_c))
+    qa = oracle.mla_absorb_q(q, w_uk, dtype="f64")
+    out = oracle.mla_unabsorb_out(o, w_uv_t, dtype="f64")
+    for b in range(B):
+        for i in range(H):
+            for a in range(d_c):  # q_abs_i = q_i W_uk^(i)^T, W_uk^(i) = w_uk[i] (d_c x d_h)
+                assert qa[b, i, a] == pytest.approx(sum(q[b, i, e] * w_uk[i, a, e]
+                                                        for e in range(d_h)), abs=1e-13)
+            for v in range(d_v):  # out_i = o_i W_uv^(i), W_uv^(i) = w_uv_t[i]^T (d_c x d_v)
+                assert out[b, i, v] == pytest.approx(sum(o[b, i, a] * w_uv_t[i, v, a]
+                                                         for a in range(d_c)), abs=1e-13)
+
+
+def test_absorb_attend_unabsorb_equals_explicit_reconstruction_per_sequence():
+    """Absorb the query, attend over the latent cache, apply W_uv: the same as
+    reconstructing every head's K and V from the latent and attending to them
+    (the pages' reconstruct-or-absorb question), for a batch of sequences."""
+    rng = np.random.default_rng(41)
+    B, H, d_c, d_h, d_r, d_v, S = 2, 4, 32, 16, 8, 16, 9
+    q_nope = rng.standard_normal((B, H, d_h))
+    q_rope = rng.standard_normal((B, H, d_r))
+    c = rng.standard_normal((B, S, d_c))
+    kr = rng.standard_normal((B, S, d_r))
+    w_uk = rng.standard_normal((H, d_c, d_h)) / math.sqrt(d_c)
+    w_uv = rng.standard_normal((H, d_c, d_v)) / math.sqrt(d_c)
+    scale = 1.0 / math.sqrt(d_h + d_r)
+    q_abs = oracle.mla_absorb_q(q_nope, w_uk, dtype="f64")
+    cache = np.concatenate([c, kr], axis=2).reshape(B * S, 1, d_c + d_r)  # block_size 1
+    bt = np.arange(B * S, dtype=np.int32).reshape(B, S)
+    lat, _ = oracle.mla_decode(q_abs, q_rope, cache, bt, np.full(B, S, np.int32), dtype="f64",
+                               scale=scale)
+    out = oracle.mla_unabsorb_out(lat.reshape(B, H, d_c), np.swapaxes(w_uv, 1, 2).copy(),
+                                  dtype="f64")
+    for b in range(B):
+        ref, _ = oracle.mla_explicit(q_nope[b], q_rope[b], c[b], kr[b], w_uk, w_uv, scale=scale)
+        np.testing.assert_allclose(out[b], ref, rtol=1e-10, atol=1e-12)
+    # sensitivity: W_uk^(i) used untransposed (square case) or heads shifted is different
+    sq = rng.standard_normal((H, d_h, d_h))
+    assert not np.allclose(oracle.mla_absorb_q(q_nope, sq, dtype="f64"),
+                           oracle.mla_absorb_q(q_nope, np.swapaxes(sq, 1, 2).copy(), dtype="f64"))
+    assert not np.allclose(q_abs, oracle.mla_absorb_q(q_nope, np.roll(w_uk, 1, axis=0),
+                                                      dtype="f64"))
+
+
+def test_absorption_reads_16bit_weights_like_their_decoded_values():
+    rng = np.random.default_rng(42)
+    q = rng.standard_normal((2, 3, 8)).astype(np.float16)
+    w = rng.standard_normal((3, 5, 8)).astype(np.float16)
+    got = oracle.mla_absorb_q(q.view(np.uint16), w.view(np.uint16), dtype="fp16")
+    ref = oracle.mla_absorb_q(q.astype(np.float64), w.astype(np.float64), dtype="f64")
+    assert np.array_equal(got, ref)
