@@ -96,6 +96,29 @@ def time_calls(call, n: int, stream, dev) -> float:
     return e0.elapsed_time(e1) / n
 
 
+def time_graph(call, n: int, stream, dev, per_graph: int = 20) -> float:
+    """Mean ms per call with `per_graph` calls captured in one CUDA graph and
+    the graph replayed: device time without the binding's per-call host cost
+    (for launch-bound kernels)."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        call()  # warm the path on the capture stream
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(per_graph):
+                call()
+    stream.wait_stream(side)
+    ms = time_calls(g.replay, max(3, n // per_graph), stream, dev) / per_graph
+    del g
+    return ms
+
+
+def head_gemm_bytes(x, w, y) -> int:
+    """Algorithmic bytes of a per-head batched GEMM: weights, input and output once."""
+    return (x.numel() + w.numel() + y.numel()) * x.element_size()
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -530,18 +553,7 @@ def main():
                              err_flag=flag)
 
         a_ms = time_calls(a_call, nf, stream, dev)
-        # The same calls captured in a CUDA graph and replayed: the device-side
-        # cost without the Python binding's per-call overhead.
-        a_graph = torch.cuda.CUDAGraph()
-        a_side = torch.cuda.Stream(dev)
-        a_side.wait_stream(stream)
-        with torch.cuda.stream(a_side):
-            a_call()  # warm the path on the capture stream
-            with torch.cuda.graph(a_graph, stream=a_side):
-                for _ in range(20):
-                    a_call()
-        stream.wait_stream(a_side)
-        ag_ms = time_calls(a_graph.replay, max(3, nf // 20), stream, dev) / 20
+        ag_ms = time_graph(a_call, nf, stream, dev)
         a_bytes = 2 * 2 * int((a_pos >= 0).sum().item()) * gx.h_kv * gx.d_head * 2
         extras["kv_append"] = {"workload": f"{GQA_WORKLOAD} new-token K/V write",
                                "us_per_call": a_ms * 1e3, "us_per_call_graph": ag_ms * 1e3,
@@ -550,7 +562,47 @@ def main():
                                "note": "launch-bound (0.5 MB per call); us_per_call includes "
                                        "the Python binding, the graph figure is device time"}
         err |= int(flag.item())
-        del a_graph
+
+    # ---------------- extra: MLA's absorption GEMMs around the latent kernel
+    # (DeepSeek-V2 shapes, random-init weights), device time from graph replay.
+    # One weight set is 17 MB, so consecutive calls cycle through 8 layers'
+    # weights (268 MB, more than L2) as a model's layers would.
+    if mx is not None and not args.no_extras:
+        n_layers = 8
+        abs_ = [synth.mla_absorb_inputs(mx.batch, seed=rank * 100 + i, device=dev)
+                for i in range(n_layers)]
+        q_abs_out = torch.empty((mx.batch, 128, 512), dtype=abs_[0].q_nope.dtype, device=dev)
+        o_out = torch.empty((mx.batch, 128, 128), dtype=abs_[0].q_nope.dtype, device=dev)
+        nf = max(3, min(K, 500))
+        layer = [0]
+
+        def next_layer():
+            layer[0] = (layer[0] + 1) % n_layers
+            return abs_[layer[0]]
+
+        def absorb_call():
+            ab = next_layer()
+            da.mla_absorb_q(ab.q_nope, ab.w_uk, out=q_abs_out, err_flag=flag)
+
+        def unabsorb_call():
+            ab = next_layer()
+            da.mla_unabsorb_out(ab.o_lat, ab.w_uv_t, out=o_out, err_flag=flag)
+
+        ab0 = abs_[0]
+        gemms = {"mla_absorb_q": (absorb_call, head_gemm_bytes(ab0.q_nope, ab0.w_uk, q_abs_out)),
+                 "mla_unabsorb_out": (unabsorb_call,
+                                      head_gemm_bytes(ab0.o_lat, ab0.w_uv_t, o_out))}
+        extras = extras or {}
+        for name, (call, nbytes) in gemms.items():
+            g_ms = time_graph(call, nf, stream, dev, per_graph=4 * n_layers)
+            gbps = nbytes / (g_ms * 1e-3) / 1e9
+            extras[name] = {"workload": f"{MLA_WORKLOAD} (B={mx.batch}, 128 heads, "
+                                        f"{n_layers} layers' weights in turn)",
+                            "us_graph": g_ms * 1e3, "bytes": nbytes, "GBps": gbps,
+                            "frac_of_hbm_peak": gbps / hbm,
+                            "flops": 2 * mx.batch * 128 * 128 * 512, "steps": nf}
+        err |= int(flag.item())
+        del abs_, q_abs_out, o_out
 
     parts_out = {}
     for name, ms in part_ms.items():

@@ -91,6 +91,10 @@ def lib() -> ctypes.CDLL:
             L.gqa_kv_append_fp8kv.restype = I
             L.mla_kv_append.argtypes = [P, P, P, P, LP]
             L.mla_kv_append.restype = I
+            L.mla_absorb_q.argtypes = [P, P, P, I, I, I, I, I, P, P]
+            L.mla_absorb_q.restype = I
+            L.mla_unabsorb_out.argtypes = [P, P, P, I, I, I, I, I, P, P]
+            L.mla_unabsorb_out.restype = I
             L.mla_decode.argtypes = [P, P, P, P, P, P, F, LP]
             L.mla_decode.restype = I
             L.gqa_decode_plan_splits.argtypes = [I, I, I, I, I, I]
@@ -396,6 +400,54 @@ def mla_kv_append(latent_new, positions, block_table, latent_cache, *, err_flag=
                              latent_cache.data_ptr(), ctypes.byref(L))
     if st != DECATTN_OK:
         raise DecAttnError("mla_kv_append", st)
+
+
+def mla_absorb_q(q_nope, w_uk, *, out=None, err_flag=None, stream=None):
+    """q_abs[b, i, :] = q_nope[b, i, :] W_uk^(i)^T through the C ABI.
+
+    q_nope [B, H, d_h]; w_uk [H, d_c, d_h] (w_uk[i] = W_uk^(i)); returns
+    q_abs [B, H, d_c], mla_decode's absorbed query.
+    """
+    _check(q_nope, "q_nope", ndim=3)
+    _check(w_uk, "w_uk", q_nope.dtype, 3)
+    if q_nope.dtype not in _DT:
+        raise TypeError("q_nope must be float16 or bfloat16")
+    B, H, d_h = q_nope.shape
+    if w_uk.shape[0] != H or w_uk.shape[2] != d_h:
+        raise ValueError("w_uk must be [H, d_c, d_h]")
+    d_c = w_uk.shape[1]
+    if out is None:
+        out = torch.empty((B, H, d_c), dtype=q_nope.dtype, device=q_nope.device)
+    _check(out, "out", q_nope.dtype, 3)
+    st = lib().mla_absorb_q(q_nope.data_ptr(), w_uk.data_ptr(), out.data_ptr(), B, H, d_h, d_c,
+                            _DT[q_nope.dtype], _ptr(err_flag), _stream_handle(stream))
+    if st != DECATTN_OK:
+        raise DecAttnError("mla_absorb_q", st)
+    return out
+
+
+def mla_unabsorb_out(o_lat, w_uv_t, *, out=None, err_flag=None, stream=None):
+    """out[b, i, :] = o_lat[b, i, :] W_uv^(i) through the C ABI.
+
+    o_lat [B, H, d_c] (mla_decode's output); w_uv_t [H, d_v, d_c] (w_uv_t[i]
+    = W_uv^(i) transposed); returns [B, H, d_v].
+    """
+    _check(o_lat, "o_lat", ndim=3)
+    _check(w_uv_t, "w_uv_t", o_lat.dtype, 3)
+    if o_lat.dtype not in _DT:
+        raise TypeError("o_lat must be float16 or bfloat16")
+    B, H, d_c = o_lat.shape
+    if w_uv_t.shape[0] != H or w_uv_t.shape[2] != d_c:
+        raise ValueError("w_uv_t must be [H, d_v, d_c]")
+    d_v = w_uv_t.shape[1]
+    if out is None:
+        out = torch.empty((B, H, d_v), dtype=o_lat.dtype, device=o_lat.device)
+    _check(out, "out", o_lat.dtype, 3)
+    st = lib().mla_unabsorb_out(o_lat.data_ptr(), w_uv_t.data_ptr(), out.data_ptr(), B, H, d_c,
+                                d_v, _DT[o_lat.dtype], _ptr(err_flag), _stream_handle(stream))
+    if st != DECATTN_OK:
+        raise DecAttnError("mla_unabsorb_out", st)
+    return out
 
 
 def mla_decode(q_absorbed, q_rope, latent_cache, block_table, seq_lens, *, scale: float,

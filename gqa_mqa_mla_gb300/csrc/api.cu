@@ -64,6 +64,23 @@ bool make_map_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, ui
                        inner, outer, row_bytes, box_inner, box_outer);
 }
 
+// 3-D tensor map over a row-major [n2, n1, n0] 16-bit tensor (n0 innermost),
+// boxes of b0 x b1 x b2 elements, 128-byte swizzle.
+bool make_map_3d(CUtensorMap* m, const void* base, bool bf16, uint64_t n0, uint64_t n1,
+                 uint64_t n2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {n0, n1, n2};
+  cuuint64_t strides[2] = {n0 * 2, n0 * n1 * 2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
   static int cache[64] = {0};
   int dev = 0;
@@ -522,6 +539,52 @@ int mla_kv_append(const void* latent_new, const int32_t* positions, const int32_
                   void* latent_cache, const decattn_launch* L) {
   return kv_append_impl(latent_new, nullptr, nullptr, nullptr, false, positions, block_table,
                         latent_cache, nullptr, kMlaWidth, kMlaWidth, true, L);
+}
+
+// MLA's absorption GEMMs: Y[b, i, :] = X[b, i, :] W_i^T for every head i.
+static int head_gemm_impl(const void* x, const void* w, void* y, int batch, int heads, int m,
+                          int k, int dtype, int* err_flag, void* stream) {
+  if (!x || !w || !y) return DECATTN_ERR_INVALID_ARG;
+  if (batch < 1 || heads < 1 || m < 1 || k < 1) return DECATTN_ERR_INVALID_ARG;
+  if (dtype != DECATTN_FP16 && dtype != DECATTN_BF16) return DECATTN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 2)) return DECATTN_ERR_INVALID_ARG;
+  if (err_flag && !aligned(err_flag, 4)) return DECATTN_ERR_INVALID_ARG;
+  if (m % 128 != 0 || k % 64 != 0 || heads > 65535) return DECATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(heads) * m > 0x7fffffffLL ||
+      static_cast<int64_t>(batch) * heads * m > (1LL << 40))
+    return DECATTN_ERR_UNSUPPORTED;
+  HeadGemmParams p{};
+  p.out = y;
+  p.err_flag = err_flag;
+  p.batch = batch;
+  p.heads = heads;
+  p.m = m;
+  p.k = k;
+  const int b16 = (batch + 15) / 16 * 16;
+  p.n_tile = b16 < 256 ? b16 : 256;
+  if ((batch + p.n_tile - 1) / p.n_tile > 65535) return DECATTN_ERR_UNSUPPORTED;
+  p.stages = k / 64 < 4 ? k / 64 : 4;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < p.n_tile) p.tmem_cols *= 2;
+  const bool bf16 = dtype == DECATTN_BF16;
+  CUtensorMap tw, tx;
+  if (!make_map_2d(&tw, w, bf16, static_cast<uint64_t>(k), static_cast<uint64_t>(heads) * m,
+                   static_cast<uint64_t>(k) * 2, 64, 128) ||
+      !make_map_3d(&tx, x, bf16, static_cast<uint64_t>(k), static_cast<uint64_t>(heads),
+                   static_cast<uint64_t>(batch), 64, 1, static_cast<uint32_t>(p.n_tile)))
+    return DECATTN_ERR_CUDA;
+  const cudaError_t e = launch_head_gemm(p, tw, tx, bf16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
+}
+
+int mla_absorb_q(const void* q_nope, const void* w_uk, void* q_abs, int batch, int n_heads,
+                 int d_h, int d_c, int dtype, int* err_flag, void* stream) {
+  return head_gemm_impl(q_nope, w_uk, q_abs, batch, n_heads, d_c, d_h, dtype, err_flag, stream);
+}
+
+int mla_unabsorb_out(const void* o_lat, const void* w_uv_t, void* out, int batch, int n_heads,
+                     int d_c, int d_v, int dtype, int* err_flag, void* stream) {
+  return head_gemm_impl(o_lat, w_uv_t, out, batch, n_heads, d_v, d_c, dtype, err_flag, stream);
 }
 
 }  // extern "C"

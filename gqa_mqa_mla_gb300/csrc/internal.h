@@ -81,6 +81,17 @@ struct AppendParams {
   int block_size, log2_block_size, num_blocks, max_blocks_per_seq;
 };
 
+// Per-head batched GEMM Y[b, i, :] = X[b, i, :] W_i^T (MLA absorption).
+struct HeadGemmParams {
+  void* out;        // [batch, heads, m] 16-bit
+  int* err_flag;
+  int batch, heads;
+  int m, k;         // W_i is [m x k]; m a multiple of 128, k of 64
+  int n_tile;       // batch rows per CTA: a multiple of 16, <= 256
+  int stages;       // K-chunk ring depth
+  int tmem_cols;    // power of two >= max(32, n_tile)
+};
+
 struct CombineParams {
   const float* part_o;
   const float* part_lse;
@@ -103,6 +114,11 @@ cudaError_t launch_mla_partial(const MlaParams& p, const CUtensorMap& tm_qa,
                                const CUtensorMap& tm_c, const CUtensorMap& tm_out,
                                const CUtensorMap& tm_po, bool bf16, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int d, bool bf16, cudaStream_t stream);
+// tm_w: 2-D [heads * m, k] 16-bit, boxes of 64 x 128; tm_x: 3-D [batch, heads,
+// k] (x = k innermost), boxes of 64 x 1 x n_tile; both 128-byte swizzle.
+cudaError_t launch_head_gemm(const HeadGemmParams& p, const CUtensorMap& tm_w,
+                             const CUtensorMap& tm_x, bool bf16, cudaStream_t stream);
+int head_gemm_smem_bytes(const HeadGemmParams& p);
 // e4m3: quantise with k_scale / v_scale (bf16 or fp16 input); else a copy.
 cudaError_t launch_append(const AppendParams& p, bool e4m3, bool bf16, cudaStream_t stream);
 cudaError_t launch_mla_combine(const MlaCombineParams& p, bool bf16, cudaStream_t stream);

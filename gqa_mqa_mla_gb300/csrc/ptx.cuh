@@ -174,6 +174,16 @@ DECATTN_DEV void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, i
       : "memory");
 }
 
+// 3-D tiled bulk tensor load global -> shared (x innermost).
+DECATTN_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // 2-D tiled bulk tensor store shared -> global, tracked by this thread's bulk
 // async-group (commit with bulk_commit_group, wait with bulk_wait_*).
 DECATTN_DEV void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {

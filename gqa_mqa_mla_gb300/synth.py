@@ -249,6 +249,29 @@ def new_token_rows(batch: int, row_shape, dtype: str = "bf16", seed: int = 0, st
     return _randn((batch, *row_shape), dtype, std, g, device)
 
 
+@dataclass
+class MLAAbsorbInputs:
+    q_nope: torch.Tensor   # [B, H, d_h]  per-head query (before absorption)
+    w_uk: torch.Tensor     # [H, d_c, d_h] W_uk^(i): latent -> key
+    o_lat: torch.Tensor    # [B, H, d_c]  softmax-weighted latent (decode output)
+    w_uv_t: torch.Tensor   # [H, d_v, d_c] W_uv^(i) transposed: latent -> value
+    dtype: str
+
+
+def mla_absorb_inputs(batch: int, heads: int = MLA_HEADS, d_h: int = 128, d_c: int = MLA_D_C,
+                      d_v: int = 128, dtype: str = "bf16", seed: int = 0,
+                      device="cpu") -> MLAAbsorbInputs:
+    """Random-init up-projection weights (std 1/sqrt(fan-in), so products stay
+    about unit-variance) and unit-variance activations."""
+    g = _gen(device, seed + 32452843)
+    return MLAAbsorbInputs(
+        q_nope=_randn((batch, heads, d_h), dtype, 1.0, g, device),
+        w_uk=_randn((heads, d_c, d_h), dtype, 1.0 / math.sqrt(d_h), g, device),
+        o_lat=_randn((batch, heads, d_c), dtype, 1.0, g, device),
+        w_uv_t=_randn((heads, d_v, d_c), dtype, 1.0 / math.sqrt(d_c), g, device),
+        dtype=dtype)
+
+
 def u16(t: torch.Tensor) -> np.ndarray:
     """Raw 16-bit storage of a fp16/bf16 tensor as a host uint16 numpy array."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)

@@ -258,6 +258,33 @@ int gqa_kv_append_fp8kv(const void* k_new, const void* v_new, const float* k_sca
 int mla_kv_append(const void* latent_new, const int32_t* positions, const int32_t* block_table,
                   void* latent_cache, const decattn_launch* launch);
 
+/*
+ * mla_absorb_q, mla_unabsorb_out -- the two GEMMs either side of mla_decode
+ * ("MQA, GQA, and MLA", section 5: q_i . k_i = x (W_q^(i) W_uk^(i)^T) c^T, so
+ * the query is multiplied by W_uk^(i)^T once and the scores are taken
+ * against the cached latent; "Why GQA's KV Cache Savings Don't Fully Reduce
+ * TPOT", "What Makes MLA Different": matrix absorption needs no per-head
+ * reconstruction at decode time).  With k_i = c W_uk^(i) and v_i = c W_uv^(i):
+ *   mla_absorb_q      q_abs[b, i, :] = q_nope[b, i, :] W_uk^(i)^T
+ *     q_nope  [batch, n_heads, d_h]      w_uk [n_heads, d_c, d_h] (w_uk[i] = W_uk^(i))
+ *     q_abs   [batch, n_heads, d_c]      (written; mla_decode's q_absorbed)
+ *   mla_unabsorb_out  out[b, i, :] = o_lat[b, i, :] W_uv^(i)
+ *     o_lat   [batch, n_heads, d_c]      (mla_decode's out)
+ *     w_uv_t  [n_heads, d_v, d_c]        (w_uv_t[i] = W_uv^(i) transposed)
+ *     out     [batch, n_heads, d_v]      (written)
+ * All tensors row-major in `dtype` (DECATTN_FP16 / DECATTN_BF16), inputs and
+ * weights 16-byte aligned; products on tensor cores with fp32 accumulation,
+ * results rounded to nearest-even.  Supported: the output width (d_c for
+ * the query, d_v for the output) a multiple of 128, the contracted width (d_h,
+ * resp. d_c) a multiple of 64; DeepSeek-V2/V3 use d_h = d_v = 128, d_c = 512.
+ * err_flag (optional) gets DECATTN_FLAG_TIMEOUT if a pipeline wait gave up;
+ * stream is a cudaStream_t (NULL: the default stream).
+ */
+int mla_absorb_q(const void* q_nope, const void* w_uk, void* q_abs, int batch, int n_heads,
+                 int d_h, int d_c, int dtype, int* err_flag, void* stream);
+int mla_unabsorb_out(const void* o_lat, const void* w_uv_t, void* out, int batch, int n_heads,
+                     int d_c, int d_v, int dtype, int* err_flag, void* stream);
+
 /* Split count the automatic planner picks (num_splits = 0).  num_sms <= 0
  * queries the current device.  Returns >= 1, or a negative status. */
 int gqa_decode_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,

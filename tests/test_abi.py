@@ -229,3 +229,35 @@ def test_kv_append_kind_specific_checks(lib):
     assert _append(lib, "fp8", L, ks=None) == binding.DECATTN_ERR_INVALID_ARG
     assert _append(lib, "fp8", L, vs=FAKE + 2) == binding.DECATTN_ERR_INVALID_ARG
     assert _append(lib, "mla", _launch(block_size=128)) == binding.DECATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("fn", ["mla_absorb_q", "mla_unabsorb_out"])
+@pytest.mark.parametrize("args,expect", [
+    (dict(x=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(w=FAKE + 8), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(y=FAKE + 1), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(batch=0), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(heads=0), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(dtype=9), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(err=FAKE + 2), binding.DECATTN_ERR_INVALID_ARG),
+])
+def test_absorption_gemm_host_checks(lib, fn, args, expect):
+    a = dict(x=FAKE, w=FAKE, y=FAKE, batch=4, heads=128, kdim=128, mdim=512,
+             dtype=binding.DECATTN_BF16, err=None)
+    if fn == "mla_unabsorb_out":
+        a.update(kdim=512, mdim=128)
+    a.update(args)
+    # argument order: (x, w, y, batch, heads, contracted width, output width, ...)
+    assert getattr(lib, fn)(a["x"], a["w"], a["y"], a["batch"], a["heads"], a["kdim"],
+                            a["mdim"], a["dtype"], a["err"], None) == expect
+
+
+def test_absorption_gemm_shape_limits(lib):
+    bf = binding.DECATTN_BF16
+    # output width must be a multiple of 128, contracted width of 64
+    assert lib.mla_absorb_q(FAKE, FAKE, FAKE, 4, 8, 128, 500, bf, None, None) == \
+        binding.DECATTN_ERR_UNSUPPORTED
+    assert lib.mla_absorb_q(FAKE, FAKE, FAKE, 4, 8, 100, 512, bf, None, None) == \
+        binding.DECATTN_ERR_UNSUPPORTED
+    assert lib.mla_unabsorb_out(FAKE, FAKE, FAKE, 4, 8, 512, 96, bf, None, None) == \
+        binding.DECATTN_ERR_UNSUPPORTED
