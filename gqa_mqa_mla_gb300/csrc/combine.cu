@@ -7,9 +7,10 @@
 // an empty range (lse = -inf) has weight 0.  A +inf lse marks a range that
 // met bad data: the whole row is written as zeros.
 //
-// One CTA of kWarps warps per row.  Warp w accumulates the splits
-// j = w, w + kWarps, ... (lane l owns the float4 columns l, l + 32, ...), with
-// several splits' loads in flight; the warps' sums meet in shared memory.
+// One warp per row, kRowsPerCta rows per CTA.  Lane l owns the float4
+// columns l, l + 32, ...; the weights are computed one per lane and
+// broadcast, and the loads of all partials are independent of each other,
+// so a row costs about two dependent global-load latencies.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -18,16 +19,15 @@ namespace {
 
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kPosInf = __builtin_huge_valf();
-constexpr int kWarps = 4;
+constexpr int kRowsPerCta = 8;
+constexpr unsigned kFull = 0xffffffffu;
 
-// Merge ns partial rows into one output row.  Partial s has its lse at
-// lse[row(s)] and its D values at po[row(s) * D].
+// Merge ns partial rows into one output row (one warp).  Partial s has its
+// lse at lse[row(s)] and its D values at po[row(s) * D].
 template <int D, bool kBF16, typename RowOf>
 __device__ __forceinline__ void merge_row(const float* lse, const float* po, RowOf row, int ns,
-                                          uint16_t* out, float4 (*red)[D / 4]) {
+                                          uint16_t* out, int lane) {
   constexpr int kVec = D / 128;  // float4 per lane
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
   float mx = kNegInf;
   bool poison = false;
   for (int s = lane; s < ns; s += 32) {
@@ -36,61 +36,56 @@ __device__ __forceinline__ void merge_row(const float* lse, const float* po, Row
     mx = fmaxf(mx, v);
   }
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  poison = __any_sync(0xffffffffu, poison);
-
+  for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+  poison = __any_sync(kFull, poison);
+  uint2* dst = reinterpret_cast<uint2*>(out);
   if (poison || mx == kNegInf) {
-    for (int c = threadIdx.x; c < D / 4; c += kWarps * 32)
-      *reinterpret_cast<uint2*>(out + c * 4) = make_uint2(0, 0);
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) dst[v * 32 + lane] = make_uint2(0, 0);
     return;
   }
-
-  float wsum = 0.f;
-  for (int s = lane; s < ns; s += 32) wsum += ex2(lse[row(s)] - mx);
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
-
   float4 acc[kVec];
 #pragma unroll
   for (int v = 0; v < kVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* po4 = reinterpret_cast<const float4*>(po);
+  float wsum = 0.f;
+  for (int s0 = 0; s0 < ns; s0 += 32) {
+    const int cnt = min(32, ns - s0);
+    // Weight of partial s0 + lane: 2^(lse - max), 0 for an empty split.
+    const float wl = lane < cnt ? ex2(lse[row(s0 + lane)] - mx) : 0.f;
+    wsum += wl;
 #pragma unroll 4
-  for (int s = warp; s < ns; s += kWarps) {
-    const float w = ex2(lse[row(s)] - mx);  // 0 for an empty split
+    for (int i = 0; i < cnt; ++i) {
+      const float w = __shfl_sync(kFull, wl, i);
+      const size_t base = row(s0 + i) * (D / 4);
 #pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-      const float4 x = po4[row(s) * (D / 4) + v * 32 + lane];
-      acc[v].x = fmaf(w, x.x, acc[v].x);
-      acc[v].y = fmaf(w, x.y, acc[v].y);
-      acc[v].z = fmaf(w, x.z, acc[v].z);
-      acc[v].w = fmaf(w, x.w, acc[v].w);
+      for (int v = 0; v < kVec; ++v) {
+        const float4 x = po4[base + v * 32 + lane];
+        acc[v].x = fmaf(w, x.x, acc[v].x);
+        acc[v].y = fmaf(w, x.y, acc[v].y);
+        acc[v].z = fmaf(w, x.z, acc[v].z);
+        acc[v].w = fmaf(w, x.w, acc[v].w);
+      }
     }
   }
 #pragma unroll
-  for (int v = 0; v < kVec; ++v) red[warp][v * 32 + lane] = acc[v];
-  __syncthreads();
+  for (int off = 16; off >= 1; off >>= 1) wsum += __shfl_xor_sync(kFull, wsum, off);
   const float inv = 1.f / wsum;
-  for (int c = threadIdx.x; c < D / 4; c += kWarps * 32) {
-    float4 t = red[0][c];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) {
-      const float4 u = red[w][c];
-      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
-    }
-    uint2 w2;
-    w2.x = pack2<kBF16>(t.x * inv, t.y * inv);
-    w2.y = pack2<kBF16>(t.z * inv, t.w * inv);
-    *reinterpret_cast<uint2*>(out + c * 4) = w2;
-  }
+  for (int v = 0; v < kVec; ++v)
+    dst[v * 32 + lane] = make_uint2(pack2<kBF16>(acc[v].x * inv, acc[v].y * inv),
+                                    pack2<kBF16>(acc[v].z * inv, acc[v].w * inv));
 }
 
 // Per-sequence split-KV partials: row r's splits are contiguous.
 template <int D, bool kBF16>
-__global__ void __launch_bounds__(kWarps * 32) lse_combine_kernel(const CombineParams p) {
-  __shared__ float4 red[kWarps][D / 4];
-  const size_t row0 = static_cast<size_t>(blockIdx.x) * p.n_split;
+__global__ void __launch_bounds__(kRowsPerCta * 32) lse_combine_kernel(const CombineParams p) {
+  const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
+  if (r >= p.rows) return;
+  const size_t row0 = static_cast<size_t>(r) * p.n_split;
   merge_row<D, kBF16>(p.part_lse, p.part_o, [row0](int s) { return row0 + s; }, p.n_split,
-                      static_cast<uint16_t*>(p.out) + static_cast<size_t>(blockIdx.x) * D, red);
+                      static_cast<uint16_t*>(p.out) + static_cast<size_t>(r) * D,
+                      threadIdx.x & 31);
 }
 
 // MLA partials of a balanced schedule: sequence b's tiles [g0, g1) were cut
@@ -99,12 +94,13 @@ __global__ void __launch_bounds__(kWarps * 32) lse_combine_kernel(const CombineP
 // b's piece in its first pair q0 is slot 2 q0 + 1 unless b starts that
 // slice, and its piece in every later pair starts that pair's slice (slot
 // 2 q).  Rows of sequences that one pair covered whole (or that have no
-// tiles) were written by the partial kernel and are skipped.  One CTA per
+// tiles) were written by the partial kernel and are skipped.  One warp per
 // (sequence, head).
 template <bool kBF16>
-__global__ void __launch_bounds__(kWarps * 32) mla_combine_kernel(const MlaCombineParams p) {
-  __shared__ float4 red[kWarps][kMlaDc / 4];
-  const int b = blockIdx.x / kMlaHeads, h = blockIdx.x % kMlaHeads;
+__global__ void __launch_bounds__(kRowsPerCta * 32) mla_combine_kernel(const MlaCombineParams p) {
+  const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
+  if (r >= p.batch * kMlaHeads) return;
+  const int b = r / kMlaHeads, h = r % kMlaHeads;
   const int T = p.ws_hdr[0];
   const int g0 = p.ws_hdr[kHdrPref + b], g1 = p.ws_hdr[kHdrPref + b + 1];
   if (g1 <= g0 || T < 1) return;
@@ -116,14 +112,14 @@ __global__ void __launch_bounds__(kWarps * 32) mla_combine_kernel(const MlaCombi
     return static_cast<size_t>(slot) * kMlaHeads + h;
   };
   merge_row<kMlaDc, kBF16>(p.part_lse, p.part_o, row, q1 - q0 + 1,
-                           static_cast<uint16_t*>(p.out) +
-                               (static_cast<size_t>(b) * kMlaHeads + h) * kMlaDc,
-                           red);
+                           static_cast<uint16_t*>(p.out) + static_cast<size_t>(r) * kMlaDc,
+                           threadIdx.x & 31);
 }
 
 template <int D, bool kBF16>
 cudaError_t launch_d(const CombineParams& p, cudaStream_t stream) {
-  lse_combine_kernel<D, kBF16><<<p.rows, kWarps * 32, 0, stream>>>(p);
+  const int ctas = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
+  lse_combine_kernel<D, kBF16><<<ctas, kRowsPerCta * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -131,11 +127,11 @@ cudaError_t launch_d(const CombineParams& p, cudaStream_t stream) {
 
 cudaError_t launch_mla_combine(const MlaCombineParams& p, bool bf16, cudaStream_t stream) {
   if (p.batch <= 0) return cudaSuccess;
-  const int rows = p.batch * kMlaHeads;
+  const int ctas = (p.batch * kMlaHeads + kRowsPerCta - 1) / kRowsPerCta;
   if (bf16)
-    mla_combine_kernel<true><<<rows, kWarps * 32, 0, stream>>>(p);
+    mla_combine_kernel<true><<<ctas, kRowsPerCta * 32, 0, stream>>>(p);
   else
-    mla_combine_kernel<false><<<rows, kWarps * 32, 0, stream>>>(p);
+    mla_combine_kernel<false><<<ctas, kRowsPerCta * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
