@@ -67,7 +67,8 @@ bool make_map_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, ui
 // 3-D tensor map over a row-major [n2, n1, n0] 16-bit tensor (n0 innermost),
 // boxes of b0 x b1 x b2 elements, 128-byte swizzle.
 bool make_map_3d(CUtensorMap* m, const void* base, bool bf16, uint64_t n0, uint64_t n1,
-                 uint64_t n2, uint32_t b0, uint32_t b1, uint32_t b2) {
+                 uint64_t n2, uint32_t b0, uint32_t b1, uint32_t b2,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {n0, n1, n2};
@@ -76,7 +77,7 @@ bool make_map_3d(CUtensorMap* m, const void* base, bool bf16, uint64_t n0, uint6
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -547,7 +548,7 @@ static int head_gemm_impl(const void* x, const void* w, void* y, int batch, int 
   if (!x || !w || !y) return DECATTN_ERR_INVALID_ARG;
   if (batch < 1 || heads < 1 || m < 1 || k < 1) return DECATTN_ERR_INVALID_ARG;
   if (dtype != DECATTN_FP16 && dtype != DECATTN_BF16) return DECATTN_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 2)) return DECATTN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16)) return DECATTN_ERR_INVALID_ARG;
   if (err_flag && !aligned(err_flag, 4)) return DECATTN_ERR_INVALID_ARG;
   if (m % 128 != 0 || k % 64 != 0 || heads > 65535) return DECATTN_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(heads) * m > 0x7fffffffLL ||
@@ -563,17 +564,25 @@ static int head_gemm_impl(const void* x, const void* w, void* y, int batch, int 
   const int b16 = (batch + 15) / 16 * 16;
   p.n_tile = b16 < 256 ? b16 : 256;
   if ((batch + p.n_tile - 1) / p.n_tile > 65535) return DECATTN_ERR_UNSUPPORTED;
-  p.stages = k / 64 < 4 ? k / 64 : 4;
+  // Enough ring stages to keep a CTA's whole K in flight where it fits: up
+  // to 8, within ~200 KB of shared memory.
+  const int stage_bytes = 128 * 128 + p.n_tile * 128;
+  int stages = (200 * 1024) / stage_bytes;
+  stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+  p.stages = k / 64 < stages ? k / 64 : stages;
   p.tmem_cols = 32;
   while (p.tmem_cols < p.n_tile) p.tmem_cols *= 2;
   const bool bf16 = dtype == DECATTN_BF16;
-  CUtensorMap tw, tx;
+  CUtensorMap tw, tx, ty;
   if (!make_map_2d(&tw, w, bf16, static_cast<uint64_t>(k), static_cast<uint64_t>(heads) * m,
                    static_cast<uint64_t>(k) * 2, 64, 128) ||
       !make_map_3d(&tx, x, bf16, static_cast<uint64_t>(k), static_cast<uint64_t>(heads),
-                   static_cast<uint64_t>(batch), 64, 1, static_cast<uint32_t>(p.n_tile)))
+                   static_cast<uint64_t>(batch), 64, 1, static_cast<uint32_t>(p.n_tile)) ||
+      !make_map_3d(&ty, y, bf16, static_cast<uint64_t>(m), static_cast<uint64_t>(heads),
+                   static_cast<uint64_t>(batch), 64, 1, static_cast<uint32_t>(p.n_tile),
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
     return DECATTN_ERR_CUDA;
-  const cudaError_t e = launch_head_gemm(p, tw, tx, bf16, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_head_gemm(p, tw, tx, ty, bf16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
 }
 

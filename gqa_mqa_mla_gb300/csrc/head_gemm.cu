@@ -13,10 +13,11 @@
 // 64-element chunks (A 16 KB + B N x 128 B per stage, 128-byte swizzle) into
 // a ring, one thread of warp 1 issues tcgen05.mma (K = 16 each) into a TMEM
 // accumulator of N fp32 columns, and warps 2-5 read it back (TMEM lane r =
-// output row m0 + r, column = batch row) and write Y[b, i, m0 + r] rounded
-// to 16 bits.  Every wait is bounded; a timeout sets the error flag, the
-// CTA stops issuing, waits for its copies and MMAs in flight, frees TMEM and
-// writes nothing.
+// output row m0 + r, column = batch row), round to 16 bits, stage the tile
+// in the (by then idle) ring as [N][128] and write Y[b, i, m0 : m0 + 128]
+// with two bulk tensor stores.  Every wait is bounded; a timeout sets the
+// error flag, the CTA stops issuing, waits for its copies and MMAs in
+// flight, frees TMEM and writes nothing.
 #include <mutex>
 
 #include "internal.h"
@@ -29,16 +30,26 @@ constexpr int kGemmThreads = 192;       // warp 0 TMA, warp 1 MMA (+ TMEM), warp
 constexpr int kChunk = 64;              // K elements per stage: one 128-byte swizzle row
 constexpr int kATileBytes = 128 * 128;  // 128 weight rows x 128 B
 
+// The ring, also the epilogue's staging area ([n_tile][128] 16-bit values).
+__host__ __device__ __forceinline__ int ring_bytes(const HeadGemmParams& p) {
+  const int ring = p.stages * (kATileBytes + p.n_tile * 128);
+  const int staging = p.n_tile * 256;
+  return ring > staging ? ring : staging;
+}
+
+// At most 79 registers, so that four CTAs fit an SM's register file (the
+// q_abs GEMM's 512 CTAs then run as one wave).
 template <bool kBF16>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, 4)
     head_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
-                     const __grid_constant__ CUtensorMap tm_x, const HeadGemmParams p) {
+                     const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_y, const HeadGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
   const int stage_bytes = kATileBytes + p.n_tile * 128;  // a multiple of 1024
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_bytes(p));
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + S);
   const uint32_t done_bar = smem_u32(bars + 2 * S);
@@ -110,20 +121,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool ok = mbar_wait_or_abort(done_bar, 0, p.err_flag, abort);
     tc_fence_after();
     if (ok && !*abort) {
+      // Every MMA has completed, so the ring is idle: stage the tile there as
+      // two boxes [n_tile][64] (output rows m0 .. m0 + 63, m0 + 64 ..), one
+      // 16-bit value per (batch row, output row); a warp's 32 lanes write 64
+      // contiguous bytes per batch row.
       const int q = warp & 3;
-      const int row = mt * 128 + q * 32 + lane;
+      const int r = q * 32 + lane;  // output row within the tile (TMEM lane)
       const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-      uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<size_t>(head) * p.m + row;
-      const size_t b_stride = static_cast<size_t>(p.heads) * p.m;
+      uint16_t* stage = reinterpret_cast<uint16_t*>(smem) + (r >> 6) * (p.n_tile * 64) + (r & 63);
       for (int j = 0; j * 32 < p.n_tile; ++j) {
         float v[32];
         tmem_ld32(tmem + lane_base + j * 32, v);
         tc_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int b = n0 + j * 32 + k;
-          if (j * 32 + k < p.n_tile && b < p.batch) out[b * b_stride] = round1<kBF16>(v[k]);
-        }
+        for (int k = 0; k < 32; ++k)
+          if (j * 32 + k < p.n_tile) stage[(j * 32 + k) * 64] = round1<kBF16>(v[k]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (warp == 2 && lane == 0) {
+        // Rows past the batch fall outside the tensor and are not written.
+        const uint32_t src = smem_u32(smem);
+        tma_store_3d(&tm_y, mt * 128, head, n0, src);
+        tma_store_3d(&tm_y, mt * 128 + 64, head, n0, src + p.n_tile * 128);
+        bulk_commit_group();
+        bulk_wait_read_all();
       }
     }
   }
@@ -133,13 +155,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, p.tmem_cols);
   }
+  if (warp == 2 && lane == 0) bulk_wait_all();
 }
 
 }  // namespace
 
 int head_gemm_smem_bytes(const HeadGemmParams& p) {
-  const int stage_bytes = kATileBytes + p.n_tile * 128;
-  const int need = 1024 + p.stages * stage_bytes + (2 * p.stages + 4) * 8;
+  const int need = 1024 + ring_bytes(p) + (2 * p.stages + 4) * 8;
   // Keep (resident CTAs) x (TMEM columns) within the SM's 512 columns: ask
   // for enough shared memory that no more than 512 / tmem_cols CTAs fit.
   const int max_ctas = 512 / p.tmem_cols;
@@ -160,13 +182,21 @@ cudaError_t allow_smem() {
   if (!done[dev]) {
     status[dev] = cudaFuncSetAttribute(head_gemm_kernel<kBF16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    // All of the SM's unified L1 / shared storage as shared memory, so that
+    // as many CTAs stay resident as their shared memory and TMEM allow (the
+    // default split left 3 of the q_abs GEMM's 42 KB CTAs per SM: two waves).
+    if (status[dev] == cudaSuccess)
+      status[dev] = cudaFuncSetAttribute(head_gemm_kernel<kBF16>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
     done[dev] = true;
   }
   return status[dev];
 }
 
 cudaError_t launch_head_gemm(const HeadGemmParams& p, const CUtensorMap& tm_w,
-                             const CUtensorMap& tm_x, bool bf16, cudaStream_t stream) {
+                             const CUtensorMap& tm_x, const CUtensorMap& tm_y, bool bf16,
+                             cudaStream_t stream) {
   if (p.batch <= 0 || p.heads <= 0) return cudaSuccess;
   const int smem = head_gemm_smem_bytes(p);
   if (smem > 232448) return cudaErrorInvalidValue;
@@ -174,9 +204,9 @@ cudaError_t launch_head_gemm(const HeadGemmParams& p, const CUtensorMap& tm_w,
   const cudaError_t e = bf16 ? allow_smem<true>() : allow_smem<false>();
   if (e != cudaSuccess) return e;
   if (bf16)
-    head_gemm_kernel<true><<<grid, kGemmThreads, smem, stream>>>(tm_w, tm_x, p);
+    head_gemm_kernel<true><<<grid, kGemmThreads, smem, stream>>>(tm_w, tm_x, tm_y, p);
   else
-    head_gemm_kernel<false><<<grid, kGemmThreads, smem, stream>>>(tm_w, tm_x, p);
+    head_gemm_kernel<false><<<grid, kGemmThreads, smem, stream>>>(tm_w, tm_x, tm_y, p);
   return cudaGetLastError();
 }
 

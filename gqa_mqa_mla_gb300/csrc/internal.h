@@ -116,8 +116,10 @@ cudaError_t launch_mla_partial(const MlaParams& p, const CUtensorMap& tm_qa,
 cudaError_t launch_combine(const CombineParams& p, int d, bool bf16, cudaStream_t stream);
 // tm_w: 2-D [heads * m, k] 16-bit, boxes of 64 x 128; tm_x: 3-D [batch, heads,
 // k] (x = k innermost), boxes of 64 x 1 x n_tile; both 128-byte swizzle.
+// tm_y: 3-D [batch, heads, m], boxes of 64 x 1 x n_tile, no swizzle.
 cudaError_t launch_head_gemm(const HeadGemmParams& p, const CUtensorMap& tm_w,
-                             const CUtensorMap& tm_x, bool bf16, cudaStream_t stream);
+                             const CUtensorMap& tm_x, const CUtensorMap& tm_y, bool bf16,
+                             cudaStream_t stream);
 int head_gemm_smem_bytes(const HeadGemmParams& p);
 // e4m3: quantise with k_scale / v_scale (bf16 or fp16 input); else a copy.
 cudaError_t launch_append(const AppendParams& p, bool e4m3, bool bf16, cudaStream_t stream);

@@ -194,6 +194,15 @@ DECATTN_DEV void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src
       : "memory");
 }
 
+// 3-D tiled bulk tensor store shared -> global (bulk async-group, as above).
+DECATTN_DEV void tma_store_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+
 DECATTN_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until every committed bulk store of this thread has read its shared

@@ -272,8 +272,8 @@ int mla_kv_append(const void* latent_new, const int32_t* positions, const int32_
  *     o_lat   [batch, n_heads, d_c]      (mla_decode's out)
  *     w_uv_t  [n_heads, d_v, d_c]        (w_uv_t[i] = W_uv^(i) transposed)
  *     out     [batch, n_heads, d_v]      (written)
- * All tensors row-major in `dtype` (DECATTN_FP16 / DECATTN_BF16), inputs and
- * weights 16-byte aligned; products on tensor cores with fp32 accumulation,
+ * All tensors row-major in `dtype` (DECATTN_FP16 / DECATTN_BF16), 16-byte
+ * aligned; products on tensor cores with fp32 accumulation,
  * results rounded to nearest-even.  Supported: the output width (d_c for
  * the query, d_v for the output) a multiple of 128, the contracted width (d_h,
  * resp. d_c) a multiple of 64; DeepSeek-V2/V3 use d_h = d_v = 128, d_c = 512.

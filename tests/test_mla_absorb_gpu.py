@@ -87,3 +87,15 @@ def test_absorb_attend_unabsorb_chain_matches_explicit_reconstruction():
         kr = np.stack([r[512:] for r in rows])
         ref, _ = oracle.mla_explicit(q_nope[b], q_rope[b], c, kr, w_uk, w_uv, scale=m.scale)
         compare(got[b], ref, f"chain b={b}", max_abs=3e-2, mean_abs=3e-3, rel_rms=2e-2)
+
+
+@pytest.mark.parametrize("batch", [256, 300])
+def test_narrow_contraction_with_a_wide_batch_tile(batch):
+    """K = 64 (one ring stage) with 256-row batch tiles: the output staging
+    area is larger than the ring and must not run into the barriers."""
+    x = synth.mla_absorb_inputs(batch, heads=4, d_h=64, d_c=256, d_v=128, seed=batch,
+                                device=DEV)
+    qa = da.mla_absorb_q(x.q_nope, x.w_uk)
+    torch.cuda.synchronize()
+    ref = oracle.mla_absorb_q(synth.u16(x.q_nope), synth.u16(x.w_uk), dtype=x.dtype)
+    compare(_flat(qa), ref.reshape(-1, ref.shape[-1]), f"K=64 B={batch}")
