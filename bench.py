@@ -47,6 +47,8 @@ GQA_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/gqa_decode.cu", "gqa_mqa_mla_gb300
                       "gqa_mqa_mla_gb300/csrc/internal.h"]
 MLA_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/mla_decode.cu", "gqa_mqa_mla_gb300/csrc/ptx.cuh",
                       "gqa_mqa_mla_gb300/csrc/internal.h"]
+GEMM_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/head_gemm.cu", "gqa_mqa_mla_gb300/csrc/ptx.cuh",
+                       "gqa_mqa_mla_gb300/csrc/internal.h"]
 
 
 # ----------------------------------------------------------------- algorithmic work
@@ -589,18 +591,22 @@ def main():
             da.mla_unabsorb_out(ab.o_lat, ab.w_uv_t, out=o_out, err_flag=flag)
 
         ab0 = abs_[0]
-        gemms = {"mla_absorb_q": (absorb_call, head_gemm_bytes(ab0.q_nope, ab0.w_uk, q_abs_out)),
+        gemms = {"mla_absorb_q": (absorb_call, head_gemm_bytes(ab0.q_nope, ab0.w_uk, q_abs_out),
+                                  "head_gemm_absorb_deepseek_v2"),
                  "mla_unabsorb_out": (unabsorb_call,
-                                      head_gemm_bytes(ab0.o_lat, ab0.w_uv_t, o_out))}
+                                      head_gemm_bytes(ab0.o_lat, ab0.w_uv_t, o_out),
+                                      "head_gemm_unabsorb_deepseek_v2")}
         extras = extras or {}
-        for name, (call, nbytes) in gemms.items():
+        for name, (call, nbytes, tkey) in gemms.items():
             g_ms = time_graph(call, nf, stream, dev, per_graph=4 * n_layers)
             gbps = nbytes / (g_ms * 1e-3) / 1e9
             extras[name] = {"workload": f"{MLA_WORKLOAD} (B={mx.batch}, 128 heads, "
                                         f"{n_layers} layers' weights in turn)",
                             "us_graph": g_ms * 1e3, "bytes": nbytes, "GBps": gbps,
                             "frac_of_hbm_peak": gbps / hbm,
-                            "flops": 2 * mx.batch * 128 * 128 * 512, "steps": nf}
+                            "flops": 2 * mx.batch * 128 * 128 * 512, "steps": nf,
+                            "traffic": (load_traffic(tkey, GEMM_KERNEL_SOURCES)
+                                        if mx.batch == 32 else None)}
         err |= int(flag.item())
         del abs_, q_abs_out, o_out
 
