@@ -113,10 +113,24 @@ def lib() -> ctypes.CDLL:
             L.decattn_mla_bytes_per_token.restype = I64
             L.decattn_status_string.argtypes = [I]
             L.decattn_status_string.restype = ctypes.c_char_p
+            L.decattn_selftest_wait_timeout.argtypes = [P, P, I, P]
+            L.decattn_selftest_wait_timeout.restype = I
             L.decattn_version.argtypes = []
             L.decattn_version.restype = I
             _lib = L
     return _lib
+
+
+def selftest_wait_timeout(limit_us: int = 1000, device="cuda"):
+    """Run the bounded-wait self test; returns (err_flag, result list of 5 ints)."""
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+    res = torch.full((5,), -1, dtype=torch.int32, device=device)
+    st = lib().decattn_selftest_wait_timeout(flag.data_ptr(), res.data_ptr(), int(limit_us),
+                                              _stream_handle(None))
+    if st != DECATTN_OK:
+        raise DecAttnError("decattn_selftest_wait_timeout", st)
+    torch.cuda.synchronize()
+    return int(flag.item()), res.cpu().tolist()
 
 
 def status_string(status: int) -> str:

@@ -194,6 +194,15 @@ const char* decattn_status_string(int status) {
 
 int decattn_version(void) { return 100; }
 
+int decattn_selftest_wait_timeout(int* err_flag, int* result, int limit_us, void* stream) {
+  if (!err_flag || !result || !aligned(err_flag, 4) || !aligned(result, 4) || limit_us < 1 ||
+      limit_us > 100000)
+    return DECATTN_ERR_INVALID_ARG;
+  const cudaError_t e = launch_wait_selftest(err_flag, result, static_cast<uint64_t>(limit_us) * 1000,
+                                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
+}
+
 int64_t decattn_kv_bytes_per_token(int n_layers, int n_kv, int d_head, int bytes) {
   if (n_layers < 0 || n_kv < 0 || d_head < 0 || bytes < 0) return -1;
   return static_cast<int64_t>(n_layers) * n_kv * d_head * 2 * bytes;

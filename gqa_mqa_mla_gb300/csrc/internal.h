@@ -125,6 +125,10 @@ int head_gemm_smem_bytes(const HeadGemmParams& p);
 cudaError_t launch_append(const AppendParams& p, bool e4m3, bool bf16, cudaStream_t stream);
 cudaError_t launch_mla_combine(const MlaCombineParams& p, bool bf16, cudaStream_t stream);
 
+// Bounded-wait self test (csrc/selftest.cu).
+cudaError_t launch_wait_selftest(int* err_flag, int* result, uint64_t limit_ns,
+                                 cudaStream_t stream);
+
 // Planner shared by the front end and the workspace query.
 int plan_gqa_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms);
 int plan_gqa_fp8_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms);

@@ -95,12 +95,13 @@ DECATTN_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity.  Returns false (and sets
 // kFlagTimeout) when the wait gave up; the caller then winds the CTA down.
-DECATTN_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* err_flag) {
+DECATTN_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* err_flag,
+                           uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   uint32_t spins = 0;
   while (!mbar_try_wait(bar, parity)) {
-    if ((++spins & 1023u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) {
+    if ((++spins & 1023u) == 0 && global_timer_ns() - t0 > limit_ns) {
       flag_error(err_flag, kFlagTimeout);
       return false;
     }
@@ -111,7 +112,8 @@ DECATTN_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* err_flag) {
 // Bounded wait that also gives up as soon as another thread of the CTA has
 // raised the shared abort word (after its own wait timed out).
 DECATTN_DEV bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, int* err_flag,
-                                    volatile int* abort, bool cluster_scope = false) {
+                                    volatile int* abort, bool cluster_scope = false,
+                                    uint64_t limit_ns = kWaitTimeoutNs) {
   auto probe = [&]() {
     return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   };
@@ -121,7 +123,7 @@ DECATTN_DEV bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, int* err_flag
   while (!probe()) {
     if ((++spins & 255u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         flag_error(err_flag, kFlagTimeout);
         *abort = 1;
         return false;

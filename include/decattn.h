@@ -314,6 +314,20 @@ int64_t decattn_mla_bytes_per_token(int n_layers, int d_c, int d_rope, int bytes
 /* Static English text for a decattn_status value; never NULL. */
 const char* decattn_status_string(int status);
 
+/* decattn_selftest_wait_timeout -- runs the bounded mbarrier waits that
+ * every kernel's pipeline uses on barriers that nothing completes, so that
+ * they give up (a diagnostic for the failure path; the pages have no
+ * counterpart).  One CTA: thread 0 waits with a limit of limit_us
+ * microseconds (1..100000) and raises the CTA's abort word; thread 32 waits
+ * with a 1000x longer limit but watches the abort word; thread 1 runs the
+ * plain bounded wait.  Device writes: *err_flag |= DECATTN_FLAG_TIMEOUT;
+ * result[0] = 1 if thread 0 gave up, result[1] = 1 if thread 32 left on the
+ * abort word (well before its own limit), result[2], result[3] = the
+ * microseconds each waited, result[4] = 1 if the plain wait gave up.
+ * err_flag, result: device pointers (result holds 5 ints); stream: a
+ * cudaStream_t or NULL. */
+int decattn_selftest_wait_timeout(int* err_flag, int* result, int limit_us, void* stream);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int decattn_version(void);
 

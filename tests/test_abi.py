@@ -261,3 +261,10 @@ def test_absorption_gemm_shape_limits(lib):
         binding.DECATTN_ERR_UNSUPPORTED
     assert lib.mla_unabsorb_out(FAKE, FAKE, FAKE, 4, 8, 512, 96, bf, None, None) == \
         binding.DECATTN_ERR_UNSUPPORTED
+
+
+def test_selftest_argument_checks(lib):
+    for args in [(None, FAKE, 100), (FAKE, None, 100), (FAKE + 2, FAKE, 100), (FAKE, FAKE, 0),
+                 (FAKE, FAKE, 100001)]:
+        assert lib.decattn_selftest_wait_timeout(args[0], args[1], args[2], None) == \
+            binding.DECATTN_ERR_INVALID_ARG
