@@ -114,11 +114,11 @@ int window_span(int max_seq_len, int window, int block_size) {
 }
 
 // Split count for `units` independent (sequence[, KV head]) work units on
-// `slots` resident CTAs.  The kernels stream HBM, so one split per unit is
-// best once there are enough CTAs to keep every SM fed (measured: the
-// 70B-shaped layer with B*h_kv = 512 units runs at the copy roofline with one
-// split); otherwise split each sequence until about two waves of CTAs exist,
-// keeping at least two 64-token tiles per split.
+// `slots` resident CTAs, for the latency-bound 8-bit-cache kernel, which
+// gains from more CTAs in flight: one split per unit once there are 1.5
+// waves of CTAs; otherwise split each sequence until about two waves exist,
+// keeping at least two 64-token tiles per split (measured on the 70B-shaped
+// layer over an e4m3 cache: 2 splits 211 us, 1 split 233 us).
 int plan_splits(int units, int max_seq_len, int slots) {
   const int tiles = max_seq_len > 0 ? (max_seq_len + kTile - 1) / kTile : 1;
   if (units < 1) units = 1;
@@ -132,20 +132,49 @@ int plan_splits(int units, int max_seq_len, int slots) {
   return resolve_splits(max_seq_len, ns, &tps);
 }
 
+// Split count for the 16-bit GQA partial kernel: fill at most ~85 % of one
+// wave of resident CTAs, with at least 8 tiles (512 tokens) per split.  A
+// wave that overflows by a few CTAs costs a second pass over the whole
+// per-CTA time, and short splits only add partials.  Measured on GB300
+// (2 CTAs per SM, 304 slots): B=1 x 8 KV heads at S=131072, 32 splits
+// 92.7 us / 38 splits 96.1 / 40 splits 133.9 / 76 splits 109.1; B=4, 8 splits
+// 314 us / 10 splits 456 / 19 splits 325; Llama-3.1-8B MQA (16 units,
+// S <= 4096), 8 splits 32 us / 32 splits 59; its GQA-8 (128 units), 2-3
+// splits 44-45 us / 5 splits 50.
+int plan_splits_one_wave(int units, int max_seq_len, int slots) {
+  const int tiles = max_seq_len > 0 ? (max_seq_len + kTile - 1) / kTile : 1;
+  if (units < 1) units = 1;
+  if (slots < 1) slots = 1;
+  int ns = static_cast<int>((static_cast<int64_t>(slots) * 85) / (100 * static_cast<int64_t>(units)));
+  int cap = tiles / 8 > 1 ? tiles / 8 : 1;
+  if (cap > DECATTN_MAX_SPLITS) cap = DECATTN_MAX_SPLITS;
+  if (ns > cap) ns = cap;
+  if (ns < 1) ns = 1;
+  int tps = 0;
+  return resolve_splits(max_seq_len, ns, &tps);
+}
+
 }  // namespace
 
 int plan_gqa_splits(int batch, int /*h_q*/, int h_kv, int max_seq_len, int num_sms) {
   // GQA partial kernel: two resident CTAs per SM (3-stage ring of 32 KB).
-  return plan_splits(batch * h_kv, max_seq_len, num_sms * 2);
+  return plan_splits_one_wave(batch * h_kv, max_seq_len, num_sms * 2);
 }
 
 int plan_gqa_fp8_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms) {
   // The 8-bit-cache kernel for 2..16 query heads per KV head runs three CTAs
-  // per SM (measured on the 70B-shaped layer: 2 splits 211 us, 1 split 233
-  // us); the other consumers, two.
+  // per SM; the other consumers, two.  Below ~0.85 of a wave of units the
+  // one-wave rule holds here too (measured at S=131072: B=1, 48 splits
+  // 70.8 us / 114 splits 88.1; B=4, 12 splits 199 us / 29 splits 231); from
+  // there on the latency-bound kernel prefers about two waves (the 70B-shaped
+  // layer, 512 units on 456 slots: 2 splits 211 us, 1 split 233 us).
   const int group = h_kv > 0 ? h_q / h_kv : 1;
   const int per_sm = (group >= 2 && group <= 16) ? 3 : 2;
-  return plan_splits(batch * h_kv, max_seq_len, num_sms * per_sm);
+  const int slots = num_sms * per_sm;
+  const int64_t units = static_cast<int64_t>(batch) * h_kv;
+  if (units * 100 < static_cast<int64_t>(slots) * 85)
+    return plan_splits_one_wave(batch * h_kv, max_seq_len, slots);
+  return plan_splits(batch * h_kv, max_seq_len, slots);
 }
 
 int plan_mla_splits(int batch, int max_seq_len, int num_sms) {
