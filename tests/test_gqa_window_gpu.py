@@ -141,3 +141,12 @@ def test_invalid_window_is_rejected():
     for w in (0, -5):
         with pytest.raises(da.DecAttnError):
             _run(x, w)
+
+
+def test_long_context_window_with_the_automatic_plan():
+    """B=1 at S=131072 under a 4096-token window: the planner sizes splits
+    for the window, not the sequence; sampled rows against the oracle."""
+    x = synth.workload_inputs("long_ctx_b1_s128k", device=DEV)
+    assert da.gqa_window_plan_splits(1, 64, 8, 131072, 4096, 16) <= \
+        da.gqa_plan_splits(1, 64, 8, 4096 + 15)
+    _check(x, 4096, n_rows=64, what="S=128k w=4096")

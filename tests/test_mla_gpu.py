@@ -181,3 +181,24 @@ def test_bad_seq_len_between_cut_sequences():
         rows = np.array([[b, i] for b in (0, 2, 3) for i in range(0, 128, 3)], np.int32)
         ref, _ = oracle_mla(x, rows)
         compare(gather_rows(out, rows), ref, f"rows around a bad length, shares={ns}")
+
+
+def test_large_batch_of_short_ragged_sequences():
+    """256 sequences of 0..600 tokens: most shares hold many whole sequences
+    (segment switches on every CTA pair), some sequences are empty."""
+    g = torch.Generator().manual_seed(77)
+    lens = torch.randint(0, 601, (256,), generator=g).tolist()
+    for b in (3, 100, 200):
+        lens[b] = 0
+    x = synth.mla_inputs(batch=256, seq_lens=lens, block_size=64, seed=78, device=DEV)
+    for ns in (0, 76, 13):
+        _check(x, ns, n_rows=512, what=f"B=256 ragged splits={ns}")
+    out = _run(x)
+    assert torch.all(out[3] == 0) and torch.all(out[200] == 0)
+
+
+def test_single_long_sequence_over_every_pair():
+    """One 65536-token sequence cut across all CTA pairs and merged by the combine."""
+    x = synth.mla_inputs(batch=1, seq_lens=[65536], block_size=64, seed=79, device=DEV)
+    _check(x, 0, n_rows=128, what="B=1 S=64k auto")
+    _check(x, 7, n_rows=64, what="B=1 S=64k 7 pairs")
