@@ -193,7 +193,10 @@ template <int MT, bool kBF16>
 struct MmaConsumer {
   static constexpr int kCacheBytes = 2;
   static constexpr int kMinBlocks = 1;
-  static constexpr int kWarps = MT <= 4 ? 4 : MT;
+  // One m-tile (up to 16 query heads): 4 warps.  Wider groups: 8 warps, so
+  // that two warps per SM sub-partition hide each other's latency (the
+  // register file then holds one CTA per SM either way).
+  static constexpr int kWarps = MT == 1 ? 4 : 8;
   static constexpr int kRowsPerWarp = 16;
   static constexpr int kWarpsPerMtile = kWarps / MT;
   static constexpr int kTokensPerWarp = kTile / kWarpsPerMtile;
