@@ -759,3 +759,65 @@ def test_absorption_reads_16bit_weights_like_their_decoded_values():
     got = oracle.mla_absorb_q(q.view(np.uint16), w.view(np.uint16), dtype="fp16")
     ref = oracle.mla_absorb_q(q.astype(np.float64), w.astype(np.float64), dtype="f64")
     assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- library cross-checks
+
+def _sdpa(q, k, v, scale):
+    """torch's scaled_dot_product_attention in fp64 on the CPU (a library
+    routine independent of the oracle): q [H, 1, d], k/v [H, S, d]."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))[None]
+    return torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v),
+                                                            scale=scale)[0].numpy()
+
+
+@pytest.mark.parametrize("h_q,h_kv,S", [(4, 4, 1), (4, 2, 3), (8, 1, 8), (6, 3, 7), (8, 2, 8)])
+def test_gqa_decode_matches_torch_sdpa_on_tiny_cases(h_q, h_kv, S):
+    rng = np.random.default_rng(50 + S)
+    bs, d = 4, 16
+    nb = math.ceil(S / bs) + 2
+    k = rng.standard_normal((nb, bs, h_kv, d))
+    v = rng.standard_normal((nb, bs, h_kv, d))
+    q = rng.standard_normal((1, h_q, d))
+    bt = rng.permutation(nb)[:math.ceil(S / bs)].astype(np.int32)[None]
+    out, lse = _gqa(q, k, v, bt, np.array([S], np.int32), 0.37)
+    kseq = np.stack([k[bt[0, t // bs], t % bs] for t in range(S)])  # [S, h_kv, d]
+    vseq = np.stack([v[bt[0, t // bs], t % bs] for t in range(S)])
+    g = h_q // h_kv
+    kk = np.repeat(kseq.transpose(1, 0, 2), g, axis=0)  # [h_q, S, d], head i -> KV head i // g
+    vv = np.repeat(vseq.transpose(1, 0, 2), g, axis=0)
+    ref = _sdpa(q[0][:, None, :], kk, vv, 0.37)[:, 0, :]
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-13)
+
+
+def test_mla_decode_matches_torch_sdpa_on_a_tiny_case():
+    """Absorbed MLA is attention with the 576-d cache row as key (the query
+    being q_abs and q_rope side by side) and its first 512 entries as value."""
+    rng = np.random.default_rng(60)
+    H, d_c, d_r, S = 4, 32, 8, 7
+    q_abs = rng.standard_normal((1, H, d_c))
+    q_rope = rng.standard_normal((1, H, d_r))
+    cache = rng.standard_normal((S, 1, d_c + d_r))
+    bt = np.arange(S, dtype=np.int32)[None]
+    out, _ = oracle.mla_decode(q_abs, q_rope, cache, bt, np.array([S], np.int32), dtype="f64",
+                               scale=0.2)
+    qcat = np.concatenate([q_abs[0], q_rope[0]], axis=1)[:, None, :]  # [H, 1, d_c + d_r]
+    keys = np.repeat(cache[:, 0][None], H, axis=0)                      # [H, S, d_c + d_r]
+    vals = keys[..., :d_c]
+    ref = _sdpa(qcat, keys, np.ascontiguousarray(vals), 0.2)[:, 0, :]
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-13)
+
+
+def test_softmax_weights_sum_to_one():
+    """out = sum_t p_t v_t with sum_t p_t = 1: appending a constant column c to
+    every value row must give exactly c in that output column (up to rounding)."""
+    rng = np.random.default_rng(61)
+    S, bs, d = 37, 8, 8
+    nb = math.ceil(S / bs)
+    k = rng.standard_normal((nb, bs, 2, d)) * 3
+    v = rng.standard_normal((nb, bs, 2, d))
+    v[..., -1] = 1.0  # the last value column is constant
+    q = rng.standard_normal((2, 4, d))
+    bt = np.stack([np.arange(nb), np.arange(nb)[::-1]]).astype(np.int32)
+    out, _ = _gqa(q, k, v, bt, np.array([S, 20], np.int32), 0.9)
+    np.testing.assert_allclose(out[:, -1], 1.0, rtol=0, atol=1e-12)
