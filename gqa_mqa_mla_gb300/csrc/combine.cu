@@ -77,9 +77,17 @@ __device__ __forceinline__ void merge_row(const float* lse, const float* po, Row
                                     pack2<kBF16>(acc[v].z * inv, acc[v].w * inv));
 }
 
+// The combines are launched as programmatic dependents of the partial
+// kernel: their CTAs may start while its last CTAs run, and wait here until
+// every partial is written (a no-op for an ordinary launch).
+__device__ __forceinline__ void wait_for_partials() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Per-sequence split-KV partials: row r's splits are contiguous.
 template <int D, bool kBF16>
 __global__ void __launch_bounds__(kRowsPerCta * 32) lse_combine_kernel(const CombineParams p) {
+  wait_for_partials();
   const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
   if (r >= p.rows) return;
   const size_t row0 = static_cast<size_t>(r) * p.n_split;
@@ -98,6 +106,7 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) lse_combine_kernel(const Com
 // (sequence, head).
 template <bool kBF16>
 __global__ void __launch_bounds__(kRowsPerCta * 32) mla_combine_kernel(const MlaCombineParams p) {
+  wait_for_partials();
   const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
   if (r >= p.batch * kMlaHeads) return;
   const int b = r / kMlaHeads, h = r % kMlaHeads;
@@ -116,11 +125,29 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) mla_combine_kernel(const Mla
                            threadIdx.x & 31);
 }
 
+// Launch with programmatic stream serialization: the kernel may begin
+// before the previous kernel on the stream has finished, and its
+// griddepcontrol.wait holds it until that kernel's memory is visible.
+template <typename Params>
+cudaError_t launch_dependent(void (*kern)(Params), int ctas, const Params& p,
+                             cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kRowsPerCta * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <int D, bool kBF16>
 cudaError_t launch_d(const CombineParams& p, cudaStream_t stream) {
   const int ctas = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
-  lse_combine_kernel<D, kBF16><<<ctas, kRowsPerCta * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(lse_combine_kernel<D, kBF16>, ctas, p, stream);
 }
 
 }  // namespace
@@ -128,11 +155,8 @@ cudaError_t launch_d(const CombineParams& p, cudaStream_t stream) {
 cudaError_t launch_mla_combine(const MlaCombineParams& p, bool bf16, cudaStream_t stream) {
   if (p.batch <= 0) return cudaSuccess;
   const int ctas = (p.batch * kMlaHeads + kRowsPerCta - 1) / kRowsPerCta;
-  if (bf16)
-    mla_combine_kernel<true><<<ctas, kRowsPerCta * 32, 0, stream>>>(p);
-  else
-    mla_combine_kernel<false><<<ctas, kRowsPerCta * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return bf16 ? launch_dependent(mla_combine_kernel<true>, ctas, p, stream)
+              : launch_dependent(mla_combine_kernel<false>, ctas, p, stream);
 }
 
 cudaError_t launch_combine(const CombineParams& p, int d, bool bf16, cudaStream_t stream) {
