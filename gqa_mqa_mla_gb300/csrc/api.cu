@@ -489,7 +489,7 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
   CUtensorMap tqa, tc, tout, tpo;
   if (!make_map_2d(&tqa, q_absorbed, bf16, kMlaDc, q_rows, kMlaDc * 2, 64, kMlaHeads) ||
       !make_map_2d(&tc, latent_cache, bf16, kMlaWidth, c_rows, kMlaWidth * 2, 64,
-                   static_cast<uint32_t>(L->block_size < 32 ? L->block_size : 32)) ||
+                   static_cast<uint32_t>(L->block_size < 64 ? L->block_size : 64)) ||
       !make_map_2d(&tout, out, bf16, kMlaDc, q_rows, kMlaDc * 2, 64, kMlaHeads))
     return DECATTN_ERR_CUDA;
   if (n_pairs > 1) {

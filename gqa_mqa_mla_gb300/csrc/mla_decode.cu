@@ -58,7 +58,7 @@ namespace decattn {
 namespace {
 
 constexpr int kT = 64;                          // tokens per tile
-constexpr int kBoxRows = 32;                    // rows per TMA box (tensor-map box height cap)
+constexpr int kBoxRows = kT;                    // rows per TMA box: a whole block up to one tile
 constexpr int kStages = 2;                      // cache ring depth
 constexpr int kChunk = 64;                      // columns per 128-byte swizzle row
 constexpr int kChunks = kMlaWidth / kChunk;     // 9 column chunks per cache row
