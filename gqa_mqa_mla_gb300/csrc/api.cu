@@ -82,6 +82,24 @@ bool make_map_3d(CUtensorMap* m, const void* base, bool bf16, uint64_t n0, uint6
   return r == CUDA_SUCCESS;
 }
 
+// 3-D tensor map with explicit byte strides for dimensions 1 and 2 (they
+// need not increase), boxes of b0 x b1 x b2 elements, 128-byte swizzle.
+bool make_map_3d_strided(CUtensorMap* m, const void* base, bool bf16, uint64_t n0, uint64_t n1,
+                         uint64_t n2, uint64_t stride1, uint64_t stride2, uint32_t b0,
+                         uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {n0, n1, n2};
+  cuuint64_t strides[2] = {stride1, stride2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
   static int cache[64] = {0};
   int dev = 0;
@@ -486,12 +504,19 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
   const bool bf16 = L->dtype == DECATTN_BF16;
   const uint64_t c_rows = static_cast<uint64_t>(L->num_blocks) * L->block_size;
   const uint64_t q_rows = static_cast<uint64_t>(L->batch) * kMlaHeads;
-  CUtensorMap tqa, tc, tout, tpo;
+  CUtensorMap tqa, tc, tc4, tout, tpo;
   if (!make_map_2d(&tqa, q_absorbed, bf16, kMlaDc, q_rows, kMlaDc * 2, 64, kMlaHeads) ||
       !make_map_2d(&tc, latent_cache, bf16, kMlaWidth, c_rows, kMlaWidth * 2, 64,
                    static_cast<uint32_t>(L->block_size < 64 ? L->block_size : 64)) ||
       !make_map_2d(&tout, out, bf16, kMlaDc, q_rows, kMlaDc * 2, 64, kMlaHeads))
     return DECATTN_ERR_CUDA;
+  if (L->block_size == 64) {
+    if (!make_map_3d_strided(&tc4, latent_cache, bf16, 64, c_rows, kMlaWidth / 64, kMlaWidth * 2,
+                             128, 64, 64, 4))
+      return DECATTN_ERR_CUDA;
+  } else {
+    tc4 = tc;  // never used: smaller blocks take one 2-D copy per chunk and block
+  }
   if (n_pairs > 1) {
     if (!make_map_2d_t(&tpo, p.part_o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, kMlaDc,
                        2ull * n_pairs * kMlaHeads, kMlaDc * 4, 32, kMlaHeads))
@@ -503,7 +528,7 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
   p.q_rope = q_rope;
 
   cudaStream_t stream = static_cast<cudaStream_t>(L->stream);
-  cudaError_t e = launch_mla_partial(p, tqa, tc, tout, tpo, bf16, stream);
+  cudaError_t e = launch_mla_partial(p, tqa, tc, tc4, tout, tpo, bf16, stream);
   if (e == cudaErrorNotSupported) return DECATTN_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DECATTN_ERR_CUDA;
   if (n_pairs > 1) {

@@ -110,9 +110,13 @@ cudaError_t launch_gqa_partial(const GqaParams& p, const CUtensorMap& tm_k,
 // min(block_size, 64) rows); q / out in fp16 or bf16.
 cudaError_t launch_gqa_partial_fp8(const GqaParams& p, const CUtensorMap& tm_k,
                                    const CUtensorMap& tm_v, bool bf16, cudaStream_t stream);
+// tm_c4: the latent cache viewed as [9 chunks][rows][64] (chunk stride 128 B,
+// row stride 1152 B), boxes of 64 x 64 rows x 4 chunks: one copy brings four
+// 64-column chunks of a 64-token tile, chunk-major; used when block_size is 64.
 cudaError_t launch_mla_partial(const MlaParams& p, const CUtensorMap& tm_qa,
-                               const CUtensorMap& tm_c, const CUtensorMap& tm_out,
-                               const CUtensorMap& tm_po, bool bf16, cudaStream_t stream);
+                               const CUtensorMap& tm_c, const CUtensorMap& tm_c4,
+                               const CUtensorMap& tm_out, const CUtensorMap& tm_po, bool bf16,
+                               cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int d, bool bf16, cudaStream_t stream);
 // tm_w: 2-D [heads * m, k] 16-bit, boxes of 64 x 128; tm_x: 3-D [batch, heads,
 // k] (x = k innermost), boxes of 64 x 1 x n_tile; both 128-byte swizzle.

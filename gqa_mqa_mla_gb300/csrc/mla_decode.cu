@@ -166,6 +166,7 @@ template <bool kBF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ CUtensorMap tm_qa,
                        const __grid_constant__ CUtensorMap tm_c,
+                       const __grid_constant__ CUtensorMap tm_c4,
                        const __grid_constant__ CUtensorMap tm_out,
                        const __grid_constant__ CUtensorMap tm_po, const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -284,6 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_c);
+      tma_prefetch_desc(&tm_c4);
       tma_prefetch_desc(&tm_qa);
       const int bs = p.block_size;
       const int rows_per_box = bs < kBoxRows ? bs : kBoxRows;
@@ -317,6 +319,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int row = bt[t >> p.log2_block_size] * bs + (t & (bs - 1));
           const uint32_t off = static_cast<uint32_t>(k * rows_per_box * 128);
           // Default L2 policy: the peer CTA loads the same tile moments later.
+          if (rows_per_box == kT) {
+            // One 64-row box per tile: a 3-D copy brings four chunks at once
+            // (this CTA's value chunks, or the other CTA's), chunk 8 (RoPE)
+            // goes with the score part.
+            const int c0 = value_part ? 4 * static_cast<int>(rank) : 4 - 4 * static_cast<int>(rank);
+            tma_load_3d(st + c0 * kCChunkBytes, &tm_c4, 0, row, c0, bar(kBarKvFull + s));
+            if (!value_part)
+              tma_load_2d(st + 8 * kCChunkBytes, &tm_c, 8 * kChunk, row, bar(kBarKvFull + s));
+            continue;
+          }
           for (int c = 0; c < kChunks; ++c) {
             const bool is_value = (c >> 2) == static_cast<int>(rank) && c < 8;
             if (is_value != value_part) continue;
@@ -758,24 +770,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <bool kBF16>
 cudaError_t launch_t(const MlaParams& p, const CUtensorMap& tqa, const CUtensorMap& tc,
-                     const CUtensorMap& tout, const CUtensorMap& tpo, cudaStream_t stream) {
+                     const CUtensorMap& tc4, const CUtensorMap& tout, const CUtensorMap& tpo,
+                     cudaStream_t stream) {
   auto kern = mla_partial_kernel<kBF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * p.n_pairs, 1);
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(tqa, tc, tout, tpo, p);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(tqa, tc, tc4, tout, tpo, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_mla_partial(const MlaParams& p, const CUtensorMap& tm_qa,
-                               const CUtensorMap& tm_c, const CUtensorMap& tm_out,
-                               const CUtensorMap& tm_po, bool bf16, cudaStream_t stream) {
+                               const CUtensorMap& tm_c, const CUtensorMap& tm_c4,
+                               const CUtensorMap& tm_out, const CUtensorMap& tm_po, bool bf16,
+                               cudaStream_t stream) {
   if (p.block_size > kT && (p.block_size % kT) != 0) return cudaErrorNotSupported;
-  return bf16 ? launch_t<true>(p, tm_qa, tm_c, tm_out, tm_po, stream)
-              : launch_t<false>(p, tm_qa, tm_c, tm_out, tm_po, stream);
+  return bf16 ? launch_t<true>(p, tm_qa, tm_c, tm_c4, tm_out, tm_po, stream)
+              : launch_t<false>(p, tm_qa, tm_c, tm_c4, tm_out, tm_po, stream);
 }
 
 }  // namespace decattn
