@@ -510,7 +510,10 @@ int mla_decode(const void* q_absorbed, const void* q_rope, const void* latent_ca
                    static_cast<uint32_t>(L->block_size < 64 ? L->block_size : 64)) ||
       !make_map_2d(&tout, out, bf16, kMlaDc, q_rows, kMlaDc * 2, 64, kMlaHeads))
     return DECATTN_ERR_CUDA;
-  if (L->block_size == 64) {
+  // check_launch caps MLA blocks at 64 rows, so block size 64 is exactly the
+  // case in which the kernel takes one 64-row box per tile and copies four
+  // chunks at once through tc4.
+  if (L->block_size >= 64) {
     if (!make_map_3d_strided(&tc4, latent_cache, bf16, 64, c_rows, kMlaWidth / 64, kMlaWidth * 2,
                              128, 64, 64, 4))
       return DECATTN_ERR_CUDA;
