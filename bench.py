@@ -279,6 +279,19 @@ def oracle_sample(gx, mx, gqa_groups, mla_seqs, seed=0):
 
 # ----------------------------------------------------------------- reference arm
 
+def workload_config(parts, gx, mx) -> dict:
+    """The workload a bench line measures (the same object on both arms):
+    shapes, cache layout and the L2 note; no choice of the implementation."""
+    return {
+        "workload": f"{GQA_WORKLOAD} + {MLA_WORKLOAD}" if len(parts) > 1 else
+        (GQA_WORKLOAD if parts == ["gqa"] else MLA_WORKLOAD),
+        "gqa": {"h_q": 64, "h_kv": 8, "d_head": 128, "batch": gx.batch, "seq_len": 8192,
+                "block_size": 16, "table": "permuted"} if gx is not None else None,
+        "mla": {"heads": 128, "d_c": 512, "d_rope": 64, "batch": mx.batch, "seq_len": 8192,
+                "block_size": 64, "table": "permuted"} if mx is not None else None,
+        "l2": "inputs larger than L2 (no flush needed)", "parallelism": "replicas"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -312,7 +325,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{GQA_WORKLOAD} + {MLA_WORKLOAD}", "parts": parts},
+            "config": workload_config(parts, gx, mx),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -614,7 +627,9 @@ def main():
     for name, ms in part_ms.items():
         gbps = part_bytes[name] / (ms * 1e-3) / 1e9
         d = {"GBps": gbps, "ms": ms, "steps_per_s": 1e3 / ms, "bytes": part_bytes[name],
-             "frac_of_hbm_peak": gbps / hbm}
+             "frac_of_hbm_peak": gbps / hbm,
+             # split-KV chunks per sequence (GQA) or CTA pairs sharing the tiles (MLA)
+             "splits": g_ns if name == "gqa" else m_ns}
         if name == "mla":
             fl = mla_flops(mx)
             tc = fl / (ms * 1e-3) / 1e12
@@ -674,16 +689,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {
-            "workload": f"{GQA_WORKLOAD} + {MLA_WORKLOAD}" if len(parts) > 1 else
-            (GQA_WORKLOAD if parts == ["gqa"] else MLA_WORKLOAD),
-            "gqa": {"h_q": 64, "h_kv": 8, "d_head": 128, "batch": gx.batch, "seq_len": 8192,
-                    "block_size": 16, "table": "permuted", "splits": g_ns} if gx is not None
-            else None,
-            "mla": {"heads": 128, "d_c": 512, "d_rope": 64, "batch": mx.batch, "seq_len": 8192,
-                    "block_size": 64, "table": "permuted", "splits": m_ns} if mx is not None
-            else None,
-            "l2": "inputs larger than L2 (no flush needed)", "parallelism": "replicas"},
+        "config": workload_config(parts, gx, mx),
         "steps_per_s": 1e3 / ms_per_step,
         "frac_of_hbm_peak": value / world / hbm,
         "parts": parts_out,
