@@ -74,8 +74,10 @@ def test_fp16_inputs():
     _check(x, what="fp16")
 
 
-def test_block_permutation_is_bit_exact():
-    x = synth.mla_inputs(batch=3, seq_lens=[500, 333, 64], block_size=16, seed=5,
+@pytest.mark.parametrize("block_size", [16, 64])
+def test_block_permutation_is_bit_exact(block_size):
+    # Block size 64 takes the four-chunk copies, 16 one copy per chunk and block.
+    x = synth.mla_inputs(batch=3, seq_lens=[500, 333, 64], block_size=block_size, seed=5,
                          table="identity", device=DEV)
     g = torch.Generator().manual_seed(11)
     perm = torch.randperm(x.num_blocks, generator=g).to(torch.int32)
