@@ -38,8 +38,8 @@
 //   warps 0-7  load Q, softmax, epilogue: warp w serves heads
 //              h = 32 (w % 4) + lane (TMEM lane h) over score columns
 //              [32 (w / 4), 32 (w / 4) + 32) and O columns of the same half;
-//              the two threads of a row swap their tile maxima through
-//              shared memory and keep separate partial row sums;
+//              both threads of a row read all 64 score columns and take
+//              the same row maximum, and keep separate partial row sums;
 //   warp 8     TMA producer for the cache ring, walking the block table;
 //   warp 9     TMEM allocator and the single MMA-issuing thread: S(j), then
 //              O += P(j) C_lat(j) once P(j) is written, then S(j + 1).
@@ -70,8 +70,8 @@ constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + kQSmemChunks * kQChunkBytes;  // 64 KB
 constexpr int kOffBars = kOffRing + kStages * kStageBytes;     // +144 KB
 constexpr int kBarBytes = 256;
-constexpr int kOffRed = kOffBars + kBarBytes;                  // row maxima / sums exchange
-constexpr int kRedBytes = 3 * 2 * kMlaHeads * 4;               // 2 max slots + 1 sum slot
+constexpr int kOffRed = kOffBars + kBarBytes;                  // row-sum exchange
+constexpr int kRedBytes = 2 * kMlaHeads * 4;                   // row sums (and the scan before)
 constexpr int kSmemBytes = 1024 + kOffRed + kRedBytes;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kThreads = kSoftmaxThreads + 64;
@@ -94,8 +94,7 @@ enum : int {
   kBarPFull = kBarSFree + 1,               // P(j) written (128 arrivals)
   kBarPvDone = kBarPFull + 1,              // O += P(j) C_lat(j) complete
   kBarQs = kBarPvDone + 1,                 // Q[:, 0:256) in shared memory (TMA)
-  kBarMax = kBarQs + 1,                    // row tile maxima exchanged (256 arrivals)
-  kBarSum = kBarMax + 1,                   // row sums exchanged (256 arrivals)
+  kBarSum = kBarQs + 1,                    // row sums exchanged (256 arrivals)
   kBarEpiW = kBarSum + 1,                  // epilogue round staged in smem (256 arrivals)
   kBarEpiR = kBarEpiW + 1,                 // epilogue round's bulk stores have read smem
   kBarEpiDone = kBarEpiR + 1,              // segment epilogue done: Q smem reusable
@@ -253,7 +252,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), kSoftmaxThreads);
     mbar_init(bar(kBarQs), 1);
-    mbar_init(bar(kBarMax), kSoftmaxThreads);
     mbar_init(bar(kBarSum), kSoftmaxThreads);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarKvFull + s), 2);
@@ -468,8 +466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int h = (warp & 3) * 32 + lane;
     const int ch = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float* red_max = reinterpret_cast<float*>(smem + kOffRed);       // [2 slots][2 halves][128]
-    float* red_sum = red_max + 2 * 2 * kMlaHeads;                    // [2 halves][128]
+    float* red_sum = reinterpret_cast<float*>(smem + kOffRed);       // [2 halves][128]
     const float scale = p.scale_log2;
     bool ok = true;
     int g = 0, k = 0, epi_round = 0;
@@ -547,35 +544,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        float s[32];
+        // This thread's 32 score columns, and the partner half's, from which
+        // both threads of the row take the same full-row maximum (no exchange).
+        float s[32], so[32];
         tmem_ld32(tmem + lane_base + kTmemS + ch * 32, s);
+        tmem_ld32(tmem + lane_base + kTmemS + (ch ^ 1) * 32, so);
         tc_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(kBarSFree));  // the MMA thread may now compute S(j + 1)
-        // Tile max of the scaled scores over this half (masked columns ignored).
+        // Tile max of the scaled scores over the row (masked columns ignored).
+        const int nvo = nval - (ch ^ 1) * 32;  // valid columns of the partner half
+        const float lowest = scale >= 0.f ? kNegInf : -kNegInf;
         if (nv < 32) {
 #pragma unroll
           for (int kk = 0; kk < 32; ++kk)
-            if (kk >= nv) s[kk] = scale >= 0.f ? kNegInf : -kNegInf;
+            if (kk >= nv) s[kk] = lowest;
         }
-        float mx[16];
+        if (nvo < 32) {
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          mx[kk] = scale >= 0.f ? fmaxf(s[kk], s[kk + 16]) : fminf(s[kk], s[kk + 16]);
+          for (int kk = 0; kk < 32; ++kk)
+            if (kk >= nvo) so[kk] = lowest;
+        }
 #pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
+        for (int kk = 0; kk < 32; ++kk)
+          so[kk] = scale >= 0.f ? fmaxf(so[kk], s[kk]) : fminf(so[kk], s[kk]);
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
           for (int kk = 0; kk < w; ++kk)
-            mx[kk] = scale >= 0.f ? fmaxf(mx[kk], mx[kk + w]) : fminf(mx[kk], mx[kk + w]);
-        float mt = mx[0] * scale;
-        if (mt != mt) mt = kNegInf;  // an all-masked half (-inf * 0 cannot occur: scale != 0)
-        // Post this half's maximum for the partner half (slot gj & 1) and
-        // go on without waiting: the exponentials below are computed against
-        // the current running max m_used, which stays valid unless a score of
-        // either half exceeds it by more than the rescale threshold -- rare
-        // after the first tile.  The exchange completes meanwhile.
-        red_max[((gj & 1) * 2 + ch) * kMlaHeads + h] = mt;
-        mbar_arrive(bar(kBarMax));
+            so[kk] = scale >= 0.f ? fmaxf(so[kk], so[kk + w]) : fminf(so[kk], so[kk + w]);
+        float mt = so[0] * scale;
+        if (mt != mt) mt = kNegInf;  // an all-masked row (-inf * 0 cannot occur: scale != 0)
         // P(j - 1) must have been consumed (and O updated) before P(j) is
         // written or O is rescaled.  (The previous segment's last PV was
         // waited for by its epilogue.)
@@ -584,31 +583,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        // p = 2^(s scale - m) (one FFMA + EX2), partial row sum, P packed two
-        // 16-bit values per TMEM column.
-        uint32_t pk[16];
-        auto exps = [&](float neg_m) -> float {
-          float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            float p0 = ex2(fmaf(s[2 * kk], scale, neg_m));
-            float p1 = ex2(fmaf(s[2 * kk + 1], scale, neg_m));
-            if (nv < 32) {
-              p0 = 2 * kk < nv ? p0 : 0.f;
-              p1 = 2 * kk + 1 < nv ? p1 : 0.f;
-            }
-            ls[kk & 3] += p0 + p1;
-            pk[kk] = pack2<kBF16>(p0, p1);
-          }
-          return (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        };
-        float lt_tile = 0.f;
-        if (m_used != kNegInf) lt_tile = exps(-m_used);
-        if (!mbar_wait_or_abort(bar(kBarMax), gj & 1, p.err_flag, abort_word)) {
-          ok = false;
-          break;
-        }
-        mt = fmaxf(mt, red_max[((gj & 1) * 2 + (ch ^ 1)) * kMlaHeads + h]);
         const bool need = mt > m_used + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? mt : m_used;
@@ -627,7 +601,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           l *= factor;
           m_used = m_new;
-          lt_tile = exps(-m_used);  // the speculative values were against the old max
+        }
+        // p = 2^(s scale - m) (one FFMA + EX2), partial row sum, P packed two
+        // 16-bit values per TMEM column.
+        uint32_t pk[16];
+        float lt_tile;
+        {
+          const float neg_m = -m_used;
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            float p0 = ex2(fmaf(s[2 * kk], scale, neg_m));
+            float p1 = ex2(fmaf(s[2 * kk + 1], scale, neg_m));
+            if (nv < 32) {
+              p0 = 2 * kk < nv ? p0 : 0.f;
+              p1 = 2 * kk + 1 < nv ? p1 : 0.f;
+            }
+            ls[kk & 3] += p0 + p1;
+            pk[kk] = pack2<kBF16>(p0, p1);
+          }
+          lt_tile = (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
         l += lt_tile;
         tmem_st16(tmem + lane_base + kTmemP + ch * 16, pk);
