@@ -97,12 +97,13 @@ enum : int {
   kBarSum = kBarQs + 1,                    // row sums exchanged (256 arrivals)
   kBarEpiW = kBarSum + 1,                  // epilogue round staged in smem (256 arrivals)
   kBarEpiR = kBarEpiW + 1,                 // epilogue round's bulk stores have read smem
-  kBarEpiDone = kBarEpiR + 1,              // segment epilogue done: Q smem reusable
+  kBarEpiDone = kBarEpiR + 1,              // segment epilogue done: the ring is free again
   kBarDrain = kBarEpiDone + 1,
   kNumBars = kBarDrain + 1
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(8 * kQChunkBytes <= kStages * kStageBytes, "epilogue staging must fit the ring");
 static_assert(kTmemP + kT / 2 <= kTmemCols, "tensor memory columns");
 
 // Work schedule.  The batch's 64-token tiles, sequence after sequence, form
@@ -342,10 +343,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (sg.kind == kSegZero) continue;
         const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
         // Q[:, 0:256) of this segment's sequence, once the previous
-        // segment's epilogue (which stages its output in the same shared
-        // memory, after that segment's last S) is done with it.
-        if (q_issued > 0 &&
-            !mbar_wait_or_abort(bar(kBarEpiDone), (q_issued - 1) & 1, p.err_flag, abort_word)) {
+        // segment's last S (tile g - 1, the last reader of the Q region) has
+        // completed: the previous epilogue stages its output in the ring, so
+        // this load overlaps it.
+        if (g > 0 && !mbar_wait_or_abort(bar(kBarKvEmptyS + (g - 1) % kStages),
+                                         ((g - 1) / kStages) & 1, p.err_flag, abort_word)) {
           ok = false;
           break;
         }
@@ -354,6 +356,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_qa, c * kChunk, sg.b * kMlaHeads,
                       bar(kBarQs));
         ++q_issued;
+        // This segment's tiles, once the previous segment's epilogue has
+        // released the ring.
+        if (q_issued > 1 &&
+            !mbar_wait_or_abort(bar(kBarEpiDone), (q_issued - 2) & 1, p.err_flag, abort_word)) {
+          ok = false;
+          break;
+        }
         const int32_t* bt = p.block_table + static_cast<size_t>(sg.b) * p.max_blocks_per_seq;
         // The tensor pipe completes PV(j - 2) before S(j - 1), so the value
         // part of tile j is requested before the score part of tile j + 1.
@@ -678,22 +687,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (partial && rank == 0 && ch == 0)
         p.part_lse[static_cast<size_t>(slot) * kMlaHeads + h] =
             seg_bad ? DECATTN_POISON_LSE : (lt > 0.f ? m_used + lg2(lt) : kNegInf);
-      // O / l leaves through shared memory and bulk tensor stores: the Q
-      // region (free: this segment's last S is done) holds four 128-row
-      // boxes of 128-byte rows, 128-byte swizzled (16-byte chunk j of row y
-      // at chunk j ^ (y % 8), conflict-free for a warp writing 32 rows).  An
-      // fp32 partial (this CTA's 256 columns = 8 boxes of 32) takes two
-      // rounds, a 16-bit output (4 boxes of 64 columns) one.
-      const int rounds = partial ? 2 : 1;
-      for (int r = 0; ok && r < rounds; ++r) {
+      // O / l leaves through shared memory and bulk tensor stores, staged in
+      // the cache ring (idle: every MMA of the segment has completed, and the
+      // producer requests the next segment's tiles only after kBarEpiDone):
+      // 128-row boxes of 128-byte rows, 128-byte swizzled (16-byte chunk j of
+      // row y at chunk j ^ (y % 8), conflict-free for a warp writing 32 rows).
+      // An fp32 partial (this CTA's 256 columns) is 8 boxes of 32 columns, a
+      // 16-bit output 4 boxes of 64; either way one round of bulk stores.
+      {
+        const int nbt = partial ? 4 : 2;  // boxes per thread
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          const int bi = ch * 2 + cc;
-          uint8_t* box = smem + kOffQ + bi * (kQChunkBytes);
+        for (int cc = 0; cc < nbt; ++cc) {
+          uint8_t* box = smem + kOffRing + (ch * nbt + cc) * kQChunkBytes;
           uint4 v[8];
           if (partial) {
             float o[32];
-            tmem_ld32(tmem + lane_base + kTmemO + ch * 128 + r * 64 + cc * 32, o);
+            tmem_ld32(tmem + lane_base + kTmemO + ch * 128 + cc * 32, o);
             tc_wait_ld();
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -723,14 +732,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) {
           ok = mbar_wait_or_abort(bar(kBarEpiW), epi_round & 1, p.err_flag, abort_word);
           if (ok) {
-            for (int bi = 0; bi < 4; ++bi) {
-              const uint32_t src = sbase + kOffQ + bi * kQChunkBytes;
+            for (int bi = 0; bi < 2 * nbt; ++bi) {
+              const uint32_t src = sbase + kOffRing + bi * kQChunkBytes;
               if (partial)
-                tma_store_2d(&tm_po, col0 + (bi >> 1) * 128 + r * 64 + (bi & 1) * 32,
-                             slot * kMlaHeads, src);
+                tma_store_2d(&tm_po, col0 + bi * 32, slot * kMlaHeads, src);
               else
-                tma_store_2d(&tm_out, col0 + (bi >> 1) * 128 + (bi & 1) * 64,
-                             static_cast<int>(head0), src);
+                tma_store_2d(&tm_out, col0 + bi * 64, static_cast<int>(head0), src);
             }
             bulk_commit_group();
             bulk_wait_read_all();
