@@ -31,7 +31,7 @@
 //   Q[:, 256:576)  TMEM, 160 columns (two 16-bit values per column)  A of S
 //   cache tiles    shared memory ring, 2 stages x 64 tokens x 576     B of S, PV
 //   P(j)           TMEM, 32 columns                                  A of PV
-//   epilogue       the Q shared-memory region, once a segment's S are done
+//   epilogue       the cache ring, idle once a segment's MMAs are done
 // TMEM columns: O [0, 256) fp32 | Q [256, 416) | S [416, 480) | P [480, 512).
 //
 // Per CTA (320 threads):
