@@ -41,8 +41,10 @@
  *   zeros to the affected output rows.  The caller reads the flag after
  *   synchronising.
  * - seq_lens[b] = 0 gives an all-zero output row (an empty softmax).
- * - Cache slots past seq_lens[b] inside a sequence's last block, and block
- *   table entries past its last block, are never read.
+ * - Cache slots past seq_lens[b] inside a sequence's last block may be
+ *   fetched with the block but never affect the result: they may hold
+ *   anything, NaN included.  Block table entries past a sequence's last
+ *   block are never read.
  */
 #ifndef DECATTN_H
 #define DECATTN_H
