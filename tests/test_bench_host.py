@@ -1,6 +1,7 @@
 """Host-side logic of bench.py that needs no GPU: the cross-rank reduction of
-the N > 1 path (two gloo ranks on CPU) and the algorithmic byte / FLOP
-accounting behind the reported KV-read GB/s and roofline."""
+the N > 1 path (two gloo ranks on CPU), the algorithmic byte / FLOP
+accounting behind the reported KV-read GB/s and roofline, and the workload
+config both arms print."""
 import os
 import socket
 
@@ -68,3 +69,19 @@ def test_mla_algorithmic_bytes_and_flops():
     x = synth.mla_inputs(batch=2, seq_lens=[100, 28], block_size=64, device="cpu")
     assert bench.mla_bytes(x) == 2 * 128 * 576 * 2 + 128 * 576 * 2 + 2 * 128 * 512 * 2
     assert bench.mla_flops(x) == 128 * 128 * (2 * 576 + 2 * 512)
+
+
+def test_workload_config_is_the_workload_only():
+    """Both arms print bench.workload_config: shapes, cache layout and the L2
+    note of the measured workload, and no choice of the implementation."""
+    cfg = bench.workload_config(["gqa", "mla"],
+                                type("G", (), {"batch": 64})(), type("M", (), {"batch": 32})())
+    assert cfg["workload"] == f"{bench.GQA_WORKLOAD} + {bench.MLA_WORKLOAD}"
+    assert cfg["gqa"] == {"h_q": 64, "h_kv": 8, "d_head": 128, "batch": 64, "seq_len": 8192,
+                          "block_size": 16, "table": "permuted"}
+    assert cfg["mla"] == {"heads": 128, "d_c": 512, "d_rope": 64, "batch": 32, "seq_len": 8192,
+                          "block_size": 64, "table": "permuted"}
+    flat = repr(cfg)
+    assert "split" not in flat and "pairs" not in flat
+    only_mla = bench.workload_config(["mla"], None, type("M", (), {"batch": 32})())
+    assert only_mla["workload"] == bench.MLA_WORKLOAD and only_mla["gqa"] is None
