@@ -116,6 +116,24 @@ def time_graph(call, n: int, stream, dev, per_graph: int = 20) -> float:
     return ms
 
 
+def time_calls_flushed(call, n: int, stream, dev, flush) -> float:
+    """Mean ms per call, each call timed alone with CUDA events on `stream`
+    right after a write of `flush` (a buffer larger than L2, written outside
+    the timed region), so that every call reads its inputs from HBM."""
+    for _ in range(3):
+        flush.fill_(1)
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i, (e0, e1) in enumerate(ev):
+        flush.fill_(i & 0x7f)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(e0.elapsed_time(e1) for e0, e1 in ev) / n
+
+
 def head_gemm_bytes(x, w, y) -> int:
     """Algorithmic bytes of a per-head batched GEMM: weights, input and output once."""
     return (x.numel() + w.numel() + y.numel()) * x.element_size()
@@ -131,7 +149,9 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-PART_EVERY = 10  # one step in this many records events between its calls
+PART_SECONDS = 0.5  # each part's own back-to-back loop runs at least this long
+PART_MIN_CALLS = 200
+PARTS_TOLERANCE = 1.03  # back-to-back parts may not overrun the whole step by more
 
 
 def source_hash(paths) -> str:
@@ -194,16 +214,17 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self, t0: float, t1: float):
+    def stop(self):
+        """Stop sampling; keep the rows for summaries of time windows."""
+        self.rows = []
         if self.proc is None:
-            return None
+            return
         time.sleep(0.12)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
@@ -211,10 +232,15 @@ class ClockSampler:
                     continue
                 try:
                     ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+                    self.rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
                 except ValueError:
                     continue
         os.unlink(self.path)
+
+    def summary(self, t0: float, t1: float):
+        """Median SM clock and active throttle reasons of the samples taken in
+        [t0, t1] (all samples when none fell inside)."""
+        rows = getattr(self, "rows", [])
         if not rows:
             return None
         inside = [r for r in rows if t0 <= r[0] <= t1]
@@ -415,17 +441,10 @@ def main():
     step_bytes = sum(part_bytes.values())
 
     K, W = args.steps, args.warmup
-    KP = (K + PART_EVERY - 1) // PART_EVERY  # steps timed part by part
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
-          for _ in range(KP)]
 
-    def step(events=None):
-        if events:
-            events[0].record(stream)
-        for i, (_, fn) in enumerate(calls):
+    def step():
+        for _, fn in calls:
             fn()
-            if events:
-                events[i + 1].record(stream)
 
     for _ in range(W):
         step()
@@ -442,24 +461,40 @@ def main():
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for k in range(K):
-        # Events between the calls (a few us per step) on every PART_EVERY-th
-        # step only: they time the parts inside the timed region while adding
-        # little to it.
-        step(ev[k // PART_EVERY] if k % PART_EVERY == 0 else None)
+    for _ in range(K):
+        step()
     end.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     if dist:
         dist.barrier()
-    clk = clocks.stop(t_wall0, t_wall1)
     elapsed_ms = start.elapsed_time(end)
-    part_ms = {name: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(KP)) / KP
-               for i, (name, _) in enumerate(calls)}
     err = int(flag.item())
     elapsed_ms = reduce_max(elapsed_ms, dist, dev)
     ms_per_step = elapsed_ms / K
     value = whole_job_gbps(step_bytes, ms_per_step, world)
+
+    # ---------------- each part in its own back-to-back loop (CUDA events on
+    # the launching stream), long enough to be timed well whatever --steps is;
+    # the clock sampler keeps running, so the loop has its own clock record.
+    part_ms, part_calls = {}, {}
+    t_parts0 = time.time()
+    for name, fn in calls:
+        est = time_calls(fn, 10, stream, dev)
+        n = int(min(20000, max(PART_MIN_CALLS, math.ceil(PART_SECONDS / max(est * 1e-3, 1e-9)))))
+        part_ms[name] = reduce_max(time_calls(fn, n, stream, dev), dist, dev)
+        part_calls[name] = n
+    t_parts1 = time.time()
+    clocks.stop()
+    clk = clocks.summary(t_wall0, t_wall1)
+    clk_parts = clocks.summary(t_parts0, t_parts1)
+    parts_sum_over_step = sum(part_ms.values()) / ms_per_step
+    parts_consistent = parts_sum_over_step <= PARTS_TOLERANCE
+    if not parts_consistent and rank == 0:
+        print(f"bench.py: WARNING: the parts timed back to back sum to {parts_sum_over_step:.3f} "
+              f"of the whole step (limit {PARTS_TOLERANCE}); the per-part roofline is suspect",
+              file=sys.stderr, flush=True)
+    err |= int(flag.item())
 
     # ---------------- end to end through the public API from pinned host buffers
     e2e = None
@@ -630,11 +665,66 @@ def main():
         err |= int(flag.item())
         del abs_, q_abs_out, o_out
 
+    # ---------------- extras: the other 16-bit GQA workloads, each call timed
+    # on its own.  Long context (B = 1 and 4 at S = 131072, inputs larger than
+    # L2, back to back) and the Llama-3.1-8B-shaped MHA / GQA-8 / MQA sweep
+    # (inputs of 671 / 168 / 21 MB, L2 flushed before every call).
+    if gx is not None and not args.no_extras:
+        extras = extras or {}
+        nf = max(PART_MIN_CALLS, min(K, 500))
+        for wl in ("long_ctx_b1_s128k", "long_ctx_b4_s128k"):
+            lx = synth.workload_inputs(wl, device=dev, seed=rank)
+            l_ns = da.gqa_plan_splits(lx.batch, lx.h_q, lx.h_kv, lx.max_seq_len)
+            l_ws = torch.empty(max(16, da.gqa_workspace_size(lx.batch, lx.h_q, l_ns)),
+                               dtype=torch.uint8, device=dev)
+            l_out = torch.empty_like(lx.q)
+
+            def l_call(lx=lx, l_ns=l_ns, l_ws=l_ws, l_out=l_out):
+                da.gqa_decode(lx.q, lx.k_cache, lx.v_cache, lx.block_table, lx.seq_lens,
+                              scale=lx.scale, max_seq_len=lx.max_seq_len, out=l_out,
+                              num_splits=l_ns, workspace=l_ws, err_flag=flag)
+
+            l_ms = time_calls(l_call, nf, stream, dev)
+            lb = gqa_bytes(lx)
+            l_gbps = lb / (l_ms * 1e-3) / 1e9
+            extras[wl] = {"workload": wl, "GBps": l_gbps, "ms": l_ms, "steps_per_s": 1e3 / l_ms,
+                          "bytes": lb, "calls_timed": nf, "frac_of_hbm_peak": l_gbps / hbm,
+                          "splits": l_ns, "l2": "inputs larger than L2, back to back"}
+            err |= int(flag.item())
+            del lx, l_ws, l_out
+        flush = torch.empty(320 << 20, dtype=torch.uint8, device=dev)
+        sweep = {}
+        for wl in ("llama31_8b_mha_b16", "llama31_8b_gqa_b16", "llama31_8b_mqa_b16"):
+            cx = synth.workload_inputs(wl, device=dev, seed=rank)
+            c_ns = da.gqa_plan_splits(cx.batch, cx.h_q, cx.h_kv, cx.max_seq_len)
+            c_ws = torch.empty(max(16, da.gqa_workspace_size(cx.batch, cx.h_q, c_ns)),
+                               dtype=torch.uint8, device=dev)
+            c_out = torch.empty_like(cx.q)
+
+            def c_call(cx=cx, c_ns=c_ns, c_ws=c_ws, c_out=c_out):
+                da.gqa_decode(cx.q, cx.k_cache, cx.v_cache, cx.block_table, cx.seq_lens,
+                              scale=cx.scale, max_seq_len=cx.max_seq_len, out=c_out,
+                              num_splits=c_ns, workspace=c_ws, err_flag=flag)
+
+            c_ms = time_calls_flushed(c_call, 200, stream, dev, flush)
+            cb = gqa_bytes(cx)
+            c_gbps = cb / (c_ms * 1e-3) / 1e9
+            sweep[f"h_kv={cx.h_kv}"] = {"workload": wl, "GBps": c_gbps, "ms": c_ms,
+                                        "steps_per_s": 1e3 / c_ms, "bytes": cb,
+                                        "calls_timed": 200, "frac_of_hbm_peak": c_gbps / hbm,
+                                        "splits": c_ns,
+                                        "flop_per_cache_byte": cx.h_q // cx.h_kv}
+            err |= int(flag.item())
+            del cx, c_ws, c_out
+        del flush
+        extras["llama31_8b_sweep"] = {"l2": "flushed (320 MB write) before every call, "
+                                            "outside the timed region", **sweep}
+
     parts_out = {}
     for name, ms in part_ms.items():
         gbps = part_bytes[name] / (ms * 1e-3) / 1e9
         d = {"GBps": gbps, "ms": ms, "steps_per_s": 1e3 / ms, "bytes": part_bytes[name],
-             "frac_of_hbm_peak": gbps / hbm,
+             "frac_of_hbm_peak": gbps / hbm, "calls_timed": part_calls[name],
              # split-KV chunks per sequence (GQA) or CTA pairs sharing the tiles (MLA)
              "splits": g_ns if name == "gqa" else m_ns}
         if name == "mla":
@@ -700,6 +790,10 @@ def main():
         "steps_per_s": 1e3 / ms_per_step,
         "frac_of_hbm_peak": value / world / hbm,
         "parts": parts_out,
+        "parts_timing": {"how": "each call in its own back-to-back loop after the main loop, "
+                                "CUDA events on the launching stream",
+                         "parts_sum_over_step": parts_sum_over_step,
+                         "consistent": parts_consistent, "clocks": clk_parts},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,

@@ -111,6 +111,8 @@ int device_sm_count() {
   return n;
 }
 
+}  // namespace
+
 // Token chunk per split: a multiple of kTile covering max_seq_len in at most
 // n_split chunks.  Returns the number of chunks actually used.
 int resolve_splits(int max_seq_len, int n_split, int* tokens_per_split) {
@@ -130,6 +132,8 @@ int window_span(int max_seq_len, int window, int block_size) {
   const int64_t span = static_cast<int64_t>(window) + (block_size < kTile ? block_size : kTile) - 1;
   return span < max_seq_len ? static_cast<int>(span) : max_seq_len;
 }
+
+namespace {
 
 // Split count for `units` independent (sequence[, KV head]) work units on
 // `slots` resident CTAs, for the latency-bound 8-bit-cache kernel, which
@@ -331,13 +335,14 @@ static int check_launch(const decattn_launch* L, bool mla) {
   return DECATTN_OK;
 }
 
-// gqa_decode and gqa_decode_fp8kv share everything but the cache element type
-// (and the 8-bit cache's per-KV-head scales).
-static int gqa_decode_impl(const void* q, const void* k_cache, const void* v_cache,
-                           const float* k_scale, const float* v_scale, bool fp8,
-                           const int32_t* block_table, const int32_t* seq_lens, void* out,
-                           int h_q, int h_kv, int d_head, float scale, int window,
-                           const decattn_launch* L) {
+}  // extern "C"
+
+namespace decattn {
+
+int gqa_check_args(const void* q, const void* k_cache, const void* v_cache,
+                   const float* k_scale, const float* v_scale, bool fp8,
+                   const int32_t* block_table, const int32_t* seq_lens, const void* out, int h_q,
+                   int h_kv, int d_head, float scale, int window, const decattn_launch* L) {
   int st = check_launch(L, false);
   if (st != DECATTN_OK) return st;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
@@ -351,8 +356,24 @@ static int gqa_decode_impl(const void* q, const void* k_cache, const void* v_cac
   if (!std::isfinite(scale)) return DECATTN_ERR_INVALID_ARG;
   if (d_head != kHeadDim) return DECATTN_ERR_UNSUPPORTED;
   if (h_q / h_kv > 64) return DECATTN_ERR_UNSUPPORTED;
-
   if (window < 0) return DECATTN_ERR_INVALID_ARG;
+  return DECATTN_OK;
+}
+
+}  // namespace decattn
+
+extern "C" {
+
+// gqa_decode and gqa_decode_fp8kv share everything but the cache element type
+// (and the 8-bit cache's per-KV-head scales).
+static int gqa_decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                           const float* k_scale, const float* v_scale, bool fp8,
+                           const int32_t* block_table, const int32_t* seq_lens, void* out,
+                           int h_q, int h_kv, int d_head, float scale, int window,
+                           const decattn_launch* L) {
+  const int st = gqa_check_args(q, k_cache, v_cache, k_scale, v_scale, fp8, block_table,
+                                seq_lens, out, h_q, h_kv, d_head, scale, window, L);
+  if (st != DECATTN_OK) return st;
   const int span = window_span(L->max_seq_len, window, L->block_size);
   int n_split = L->num_splits;
   if (n_split == 0) {

@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "decattn.h"
+
 namespace decattn {
 
 constexpr int kHeadDim = 128;      // GQA head dimension supported
@@ -132,6 +134,19 @@ cudaError_t launch_mla_combine(const MlaCombineParams& p, bool bf16, cudaStream_
 // Bounded-wait self test (csrc/selftest.cu).
 cudaError_t launch_wait_selftest(int* err_flag, int* result, uint64_t limit_ns,
                                  cudaStream_t stream);
+
+// Token chunk per split: a multiple of kTile covering max_seq_len in at most
+// n_split chunks.  Returns the number of chunks actually used.
+int resolve_splits(int max_seq_len, int n_split, int* tokens_per_split);
+// The longest token range a sliding window of `window` tokens streams
+// (max_seq_len when window <= 0).
+int window_span(int max_seq_len, int window, int block_size);
+// gqa_decode's host-side argument checks, in its order (no CUDA call):
+// DECATTN_OK, or the status the call would return.
+int gqa_check_args(const void* q, const void* k_cache, const void* v_cache,
+                   const float* k_scale, const float* v_scale, bool fp8,
+                   const int32_t* block_table, const int32_t* seq_lens, const void* out, int h_q,
+                   int h_kv, int d_head, float scale, int window, const decattn_launch* L);
 
 // Planner shared by the front end and the workspace query.
 int plan_gqa_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms);

@@ -19,7 +19,9 @@
 //     each other's results; serialise them;
 //   * the first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current); make that first call
-//     before any stream capture;
+//     before any stream capture.  The address is kept for the life of the
+//     process: a device reset (cudaDeviceReset, or a reset of the primary
+//     context) is not supported afterwards;
 //   * the array keeps the previous call's contents; nothing in it needs to
 //     start at zero (each call overwrites every partial it later reads).
 #include <mutex>
@@ -60,17 +62,23 @@ extern "C" {
 int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_table, const int32_t* seq_lens, void* out, int h_q,
                        int h_kv, int d_head, float scale, const decattn_launch* launch) {
-  if (!launch) return DECATTN_ERR_INVALID_ARG;
-  if (launch->batch < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 || d_head < 1 ||
-      launch->max_seq_len < 0 || launch->num_splits < 0 ||
-      launch->num_splits > DECATTN_MAX_SPLITS)
-    return DECATTN_ERR_INVALID_ARG;
+  // gqa_decode's own argument checks first, so that a bad argument gets the
+  // status gqa_decode would return for it.
+  const int st = decattn::gqa_check_args(q, k_cache, v_cache, nullptr, nullptr, false,
+                                         block_table, seq_lens, out, h_q, h_kv, d_head, scale,
+                                         0, launch);
+  if (st != DECATTN_OK) return st;
   int n_split = launch->num_splits;
   if (n_split == 0) {
     n_split = gqa_decode_plan_splits(launch->batch, h_q, h_kv, d_head, launch->max_seq_len, 0);
     if (n_split < 0) return n_split;
   }
-  const size_t need = gqa_decode_workspace_size(launch->batch, h_q, d_head, n_split);
+  // The scratch a plan needs depends on the split count gqa_decode will
+  // actually run: a requested count is cut to the number of 64-token tiles
+  // of the longest sequence (one split needs no scratch at all).
+  int tokens_per_split = 0;
+  const int eff = decattn::resolve_splits(launch->max_seq_len, n_split, &tokens_per_split);
+  const size_t need = gqa_decode_workspace_size(launch->batch, h_q, d_head, eff);
   if (need > decattn::kNoallocScratchBytes) return DECATTN_ERR_WORKSPACE;
   void* scratch = decattn::scratch_for_current_device();
   if (!scratch) return DECATTN_ERR_CUDA;

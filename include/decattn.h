@@ -141,7 +141,12 @@ int gqa_decode(const void* q, const void* k_cache, const void* v_cache,
  *   - All calls on a device share the array: calls that may overlap on the
  *     GPU (unordered streams) race; serialise them.
  *   - The first call on a device looks up the array's address with that
- *     device current; make it before any stream capture.
+ *     device current; make it before any stream capture.  The address is
+ *     kept for the life of the process, so a device reset (cudaDeviceReset
+ *     or a primary-context reset) is not supported after that first call.
+ *   - The scratch check uses the split count gqa_decode actually runs (a
+ *     requested count is cut to the 64-token tiles of max_seq_len), and it
+ *     comes after gqa_decode's own argument checks.
  *   - Nothing in the array needs to start at zero; its contents after a call
  *     are unspecified.
  */
@@ -299,7 +304,10 @@ int mla_decode_plan_splits(int batch, int max_seq_len, int num_sms);
 int gqa_decode_window_plan_splits(int batch, int h_q, int h_kv, int d_head, int max_seq_len,
                                   int window, int block_size, int kv_bytes, int num_sms);
 
-/* Workspace bytes needed for num_splits (>= 1): fp32 partial outputs and
+/* Helpers of the interface with no defining passage on the pages (workspace
+ * sizes, status text, version): conveniences of this C ABI.
+ *
+ * Workspace bytes needed for num_splits (>= 1): fp32 partial outputs and
  * log-sum-exps (GQA: one per split per row; MLA: two per share, plus a
  * per-sequence tile table).  0 when num_splits == 1.  Returns 0 for invalid
  * arguments as well; pure host arithmetic, no CUDA call. */

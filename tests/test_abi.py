@@ -133,6 +133,54 @@ def test_gqa_host_checks(lib, case, expect):
     assert _gqa(lib, L, **case) == expect
 
 
+def _gqa_noalloc(lib, L, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, out=FAKE, h_q=8, h_kv=2,
+                 d=128, scale=0.088):
+    fn = lib.gqa_decode_noalloc
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [P, P, P, P, P, P, I, I, I, F, ctypes.POINTER(binding.Launch)]
+    fn.restype = I
+    return fn(q, k, v, bt, sl, out, h_q, h_kv, d, scale, None if L is None else ctypes.byref(L))
+
+
+# The no-allocation variant runs gqa_decode's argument checks before its
+# scratch-size check, so every bad argument gets gqa_decode's status.
+@pytest.mark.parametrize("case,expect", [
+    (dict(L=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(q=None), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(h_q=9, h_kv=2), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(num_splits=-1)), binding.DECATTN_ERR_INVALID_ARG),
+    (dict(L=dict(max_seq_len=257)), binding.DECATTN_ERR_INVALID_ARG),
+    # a plan far beyond the 8 MiB scratch, with an unsupported head size:
+    # the head size decides the status
+    (dict(d=64, h_q=64, h_kv=8, L=dict(batch=64, max_seq_len=8192, max_blocks_per_seq=512,
+                                       num_blocks=1 << 15, num_splits=64)),
+     binding.DECATTN_ERR_UNSUPPORTED),
+    (dict(h_q=256, h_kv=2, L=dict(batch=64, max_seq_len=8192, max_blocks_per_seq=512,
+                                  num_blocks=1 << 15, num_splits=64)),
+     binding.DECATTN_ERR_UNSUPPORTED),
+    # the same plan with valid arguments needs 135 MB of scratch
+    (dict(h_q=64, h_kv=8, L=dict(batch=64, max_seq_len=8192, max_blocks_per_seq=512,
+                                 num_blocks=1 << 15, num_splits=64)),
+     binding.DECATTN_ERR_WORKSPACE),
+])
+def test_gqa_noalloc_host_checks(lib, case, expect):
+    case = dict(case)
+    L = case.pop("L", {})
+    L = None if L is None else _launch(**L)
+    assert _gqa_noalloc(lib, L, **case) == expect
+
+
+def test_gqa_noalloc_sizes_scratch_by_the_splits_it_runs(lib):
+    # 64 splits requested on one-tile sequences run as a single split, which
+    # needs no scratch: the call must not be refused for scratch (with no GPU
+    # here it reaches the device lookup and reports a CUDA status instead).
+    L = _launch(batch=64, max_seq_len=64, max_blocks_per_seq=4, num_blocks=256, num_splits=64)
+    st = _gqa_noalloc(lib, L, h_q=64, h_kv=8)
+    assert st != binding.DECATTN_ERR_WORKSPACE
+    assert binding.gqa_workspace_size(64, 64, 64) > 8 << 20
+
+
 @pytest.mark.parametrize("case,expect", [
     (dict(L=None), binding.DECATTN_ERR_INVALID_ARG),
     (dict(qa=None), binding.DECATTN_ERR_INVALID_ARG),
