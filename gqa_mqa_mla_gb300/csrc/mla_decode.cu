@@ -14,35 +14,60 @@
 // (see the work schedule below).  The fp32 O accumulator for 128 heads x 512
 // columns would fill all of one SM's tensor memory, so CTA r accumulates only
 // O[:, 256 r : 256 r + 256].  Both CTAs compute the full score tile
-// S = Q C^T (the same MMA sequence on the same bytes, hence the same bits)
-// and the same online softmax, so they need to exchange nothing; the cluster
-// only co-schedules the pair so that the second load of every cache tile is
-// an L2 hit.  The redundant score GEMM costs 1.44x the minimum tensor work.
+// S = Q C^T and the same online softmax, so they need to exchange nothing;
+// the cluster only co-schedules the pair so that the second load of every
+// cache tile is an L2 hit.  The redundant score GEMM costs 1.44x the minimum
+// tensor work.  (Each CTA sums the 576 dimensions in its own chunk order, so
+// the two CTAs' scores may differ in the last bit; each CTA normalises its
+// own columns with its own row sums.)
 //
-// Tile width: a chain of tcgen05.mma (M = 128, K = 16, bf16) into one
-// accumulator costs ~58 SM cycles per instruction for any N <= 64 and only
-// N >= 128 reaches the full tensor rate (measured on GB300: ~1.1k / 2.2k /
-// 3.9k MAC per cycle for N = 32 / 64 / 128).  The score GEMM's N is the
-// token count of a tile, so tiles are 64 tokens, the widest that fits tensor
-// memory next to O and Q.
+// Tensor-core costs that shape the kernel (measured on GB300 with M = 128,
+// K = 16, bf16): one issuing thread cannot issue tcgen05.mma faster than one
+// per ~49 cycles (A in TMEM) or ~54 cycles (A in shared memory), whatever N
+// is up to 64, while the tensor pipe itself finishes an N = 64 MMA in 32
+// cycles (A in TMEM; 48 with A in shared memory, bound by shared-memory
+// bandwidth) and an N = 256 MMA in 128.  So the score chain (36 MMAs of
+// N = 64 per tile) is bound by its issue rate, and the value GEMM is issued
+// by a second thread: O += P(j) C_lat(j) runs on the tensor pipe while the
+// first thread issues S(j + 1), which itself runs while the softmax warps
+// work on tile j.
 //
+// Chunks: the 576 columns are nine 64-column chunks; CTA r's value chunks are
+// 4r..4r+3 (latent columns [256 r, 256 r + 256)), its score chunks the other
+// five.  Every CTA keeps its chunks in "position" order: positions 0-4 hold
+// the score chunks (4-4r..7-4r, then the RoPE chunk 8) and positions 5-8 the
+// value chunks, so that one instruction sequence serves both CTAs.
 // Operand placement (per CTA):
-//   Q[:, 0:256)    shared memory (TMA), 128-byte swizzled K-major      A of S
-//   Q[:, 256:576)  TMEM, 160 columns (two 16-bit values per column)  A of S
-//   cache tiles    shared memory ring, 2 stages x 64 tokens x 576     B of S, PV
-//   P(j)           TMEM, 32 columns                                  A of PV
-//   epilogue       the cache ring, idle once a segment's MMAs are done
-// TMEM columns: O [0, 256) fp32 | Q [256, 416) | S [416, 480) | P [480, 512).
+//   Q, positions 0-4   TMEM, 160 columns (two 16-bit values per column)  A of S
+//   Q, positions 5-8   shared memory (TMA), 128-byte swizzled K-major    A of S
+//   cache tiles        shared memory ring, 2 stages x 64 tokens x 9     B of S;
+//                      chunk slots in position order                    positions 5-8: B of PV
+//   P(j)               TMEM, 32 columns                                 A of PV
+//   epilogue           the ring stage of the segment's last tile
+// TMEM columns: O [0, 256) | Q [256, 416) | S [416, 480) | P [480, 512).
+// While an MMA runs, threads touch only TMEM columns it neither reads nor
+// writes: S(j + 1) (Q, S) runs while the softmax writes P(j) and rescales O;
+// O += P(j) C(j) (P, O) runs while the softmax reads S(j + 1); O is rescaled,
+// and P(j + 1) written, only after O += P(j) C(j) has completed.
 //
-// Per CTA (320 threads):
+// Per CTA (352 threads):
 //   warps 0-7  load Q, softmax, epilogue: warp w serves heads
 //              h = 32 (w % 4) + lane (TMEM lane h) over score columns
 //              [32 (w / 4), 32 (w / 4) + 32) and O columns of the same half;
 //              both threads of a row read all 64 score columns and take
 //              the same row maximum, and keep separate partial row sums;
 //   warp 8     TMA producer for the cache ring, walking the block table;
-//   warp 9     TMEM allocator and the single MMA-issuing thread: S(j), then
-//              O += P(j) C_lat(j) once P(j) is written, then S(j + 1).
+//   warp 9     TMEM allocator; one thread issues the score GEMMs;
+//   warp 10    one thread issues the value GEMMs.
+//
+// Ring: a stage holds all 9 column chunks of a 64-token tile.  This CTA's 4
+// value chunks (latent columns [256 r, 256 r + 256)) stay until O += P C
+// has read them; the other 5 ("score chunks") are read by S only and are
+// refilled as soon as S(j) completes.  Each CTA's score chain takes its score
+// chunks first and its value chunks last, with a full barrier for each part,
+// so that a value part refilled only after O += P(j - 2) C(j - 2) is needed
+// as late as possible.  The CTA of rank 0 also pulls tiles into L2 two tiles
+// ahead of their loads.
 //
 // Online softmax in the log2 domain with lazy rescaling: the running max
 // used for the exponentials only moves (and O is rescaled in TMEM) when a new
@@ -62,7 +87,8 @@ constexpr int kBoxRows = kT;                    // rows per TMA box: a whole blo
 constexpr int kStages = 2;                      // cache ring depth
 constexpr int kChunk = 64;                      // columns per 128-byte swizzle row
 constexpr int kChunks = kMlaWidth / kChunk;     // 9 column chunks per cache row
-constexpr int kQSmemChunks = 4;                 // Q columns [0, 256) in shared memory
+constexpr int kQSmemChunks = 4;                 // Q positions 5-8 (value chunks) in shared memory
+constexpr int kValueSlot = 5;                   // ring slot (position) of the first value chunk
 constexpr int kQChunkBytes = kMlaHeads * 128;   // [128 heads][64 cols] = 16 KB
 constexpr int kCChunkBytes = kT * 128;          // [64 tokens][64 cols] = 8 KB
 constexpr int kStageBytes = kChunks * kCChunkBytes;  // 72 KB
@@ -74,36 +100,40 @@ constexpr int kOffRed = kOffBars + kBarBytes;                  // row-sum exchan
 constexpr int kRedBytes = 2 * kMlaHeads * 4;                   // row sums (and the scan before)
 constexpr int kSmemBytes = 1024 + kOffRed + kRedBytes;
 constexpr int kSoftmaxThreads = 256;
-constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kWarpProducer = 8, kWarpMmaS = 9, kWarpMmaPv = 10;
+constexpr int kThreads = kSoftmaxThreads + 96;
 constexpr int kTmemCols = 512;
 constexpr int kTmemO = 0;
-constexpr int kTmemQ = 256;                     // Q columns [256, 576): 160 TMEM columns
+constexpr int kTmemQ = 256;                     // Q positions 0-4: 160 TMEM columns
 constexpr int kTmemS = 416;                     // S tile: 64 columns fp32
 constexpr int kTmemP = 480;                     // P tile: 64 bf16 = 32 columns
+constexpr int kEpiBoxes = 4;                    // 16 KB output boxes staged per round
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when p could exceed 2^8
 
 // mbarrier slots (8 bytes each) inside the barrier area
 enum : int {
-  kBarQ = 0,                               // Q[:, 256:576) in TMEM (128 arrivals)
-  kBarKvFull = 1,                          // kStages: cache tile landed (2 arrivals)
-  kBarKvEmptyS = kBarKvFull + kStages,     // kStages: score-only chunks consumed by S
-  kBarKvEmptyV = kBarKvEmptyS + kStages,   // kStages: value chunks consumed by PV
-  kBarSFull = kBarKvEmptyV + kStages,      // S(j) computed
-  kBarSFree = kBarSFull + 1,               // S(j) read by the softmax (128 arrivals)
-  kBarPFull = kBarSFree + 1,               // P(j) written (128 arrivals)
+  kBarQ = 0,                               // Q[:, 256:576) in TMEM (256 arrivals)
+  kBarFullS = 1,                           // kStages: score chunks landed (TMA bytes)
+  kBarFullV = kBarFullS + kStages,         // kStages: value chunks landed (TMA bytes)
+  kBarEmptyS = kBarFullV + kStages,        // kStages: score chunks free again
+  kBarEmptyV = kBarEmptyS + kStages,       // kStages: value chunks free again
+  kBarSFull = kBarEmptyV + kStages,        // S(j) computed
+  kBarSFree = kBarSFull + 1,               // S(j) read by the softmax (256 arrivals)
+  kBarPFull = kBarSFree + 1,               // P(j) written (256 arrivals)
   kBarPvDone = kBarPFull + 1,              // O += P(j) C_lat(j) complete
   kBarQs = kBarPvDone + 1,                 // Q[:, 0:256) in shared memory (TMA)
-  kBarSum = kBarQs + 1,                    // row sums exchanged (256 arrivals)
+  kBarQFree = kBarQs + 1,                  // a segment's last S done: Q may be replaced
+  kBarSum = kBarQFree + 1,                 // row sums exchanged (256 arrivals)
   kBarEpiW = kBarSum + 1,                  // epilogue round staged in smem (256 arrivals)
   kBarEpiR = kBarEpiW + 1,                 // epilogue round's bulk stores have read smem
-  kBarEpiDone = kBarEpiR + 1,              // segment epilogue done: the ring is free again
-  kBarDrain = kBarEpiDone + 1,
-  kNumBars = kBarDrain + 1
+  kBarDrainS = kBarEpiR + 1,               // every score MMA complete
+  kBarDrainP = kBarDrainS + 1,             // every value MMA complete
+  kNumBars = kBarDrainP + 1
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(8 * kQChunkBytes <= kStages * kStageBytes, "epilogue staging must fit the ring");
+static_assert(kEpiBoxes * kQChunkBytes <= kStageBytes, "epilogue staging must fit one stage");
 static_assert(kTmemP + kT / 2 <= kTmemCols, "tensor memory columns");
 
 // Work schedule.  The batch's 64-token tiles, sequence after sequence, form
@@ -132,8 +162,24 @@ __device__ __forceinline__ int seq_tiles(const MlaParams& p, int len) {
   return (len < 0 || len > p.max_seq_len) ? 0 : (len + kT - 1) / kT;
 }
 
+// Cache / Q chunk held at position pos by the CTA of rank r (positions 0-4:
+// its score chunks, 5-8: its value chunks), and the position of chunk c.
+__host__ __device__ constexpr int chunk_at(int r, int pos) {
+  return pos < 4 ? 4 - 4 * r + pos : (pos == 4 ? 8 : 4 * r + pos - kValueSlot);
+}
+__host__ __device__ constexpr int position_of(int r, int c) {
+  return c == 8 ? 4 : ((c >> 2) == r ? kValueSlot + (c & 3) : (c & 3));
+}
+static_assert(chunk_at(0, 0) == 4 && chunk_at(0, 4) == 8 && chunk_at(0, 5) == 0 && chunk_at(0, 8) == 3,
+              "position order, CTA 0");
+static_assert(chunk_at(1, 0) == 0 && chunk_at(1, 4) == 8 && chunk_at(1, 5) == 4 && chunk_at(1, 8) == 7,
+              "position order, CTA 1");
+static_assert(position_of(0, chunk_at(0, 6)) == 6 && position_of(1, chunk_at(1, 2)) == 2 &&
+                  position_of(1, chunk_at(1, 7)) == 7 && position_of(0, chunk_at(0, 4)) == 4,
+              "positions invert the chunk order");
+
 // Next segment of this pair's slice (every role walks the same sequence).
-__device__ bool next_seg(const MlaParams& p, const Sched& sc, Cursor& cur, Seg& sg) {
+__device__ __noinline__ bool next_seg(const MlaParams& p, const Sched& sc, Cursor& cur, Seg& sg) {
   while (cur.b < p.batch) {
     const int b = cur.b, pref = cur.pref;
     const int len = p.seq_lens[b];
@@ -160,6 +206,99 @@ __device__ bool next_seg(const MlaParams& p, const Sched& sc, Cursor& cur, Seg& 
     return true;
   }
   return false;
+}
+
+// ---------------- producer helpers (out of line: the producer's code is
+// kept small so that the four roles' loops share the SM's instruction cache)
+struct Producer {
+  const MlaParams* p;
+  const CUtensorMap* tm_c;
+  const CUtensorMap* tm_c4;
+  volatile int* abort;
+  uint32_t ring, bar0;  // shared-memory addresses: ring base, barrier area
+  int rank, rows_per_box;
+};
+
+// Request one part of ring tile gi (tokens [t0, t0 + nval) of the sequence
+// whose block-table row is bt): the 4 value chunks of this CTA (latent columns
+// [256 r, 256 r + 256)) or the 5 others.  Waits until the part's previous
+// readers have released the stage.  Returns false when the wait gave up.
+__device__ __noinline__ bool load_part(const Producer& pr, const int32_t* bt, int t0, int nval,
+                                       int gi, bool value_part) {
+  const MlaParams& p = *pr.p;
+  const int s = gi % kStages;
+  const uint32_t empty = pr.bar0 + 8u * static_cast<uint32_t>((value_part ? kBarEmptyV : kBarEmptyS) + s);
+  if (!mbar_wait_or_abort(empty, ((gi / kStages) & 1) ^ 1, p.err_flag, pr.abort)) return false;
+  const int bs = p.block_size, rpb = pr.rows_per_box;
+  const int nbox = (nval + rpb - 1) / rpb;
+  const uint32_t st = pr.ring + s * kStageBytes;
+  const uint32_t full = pr.bar0 + 8u * static_cast<uint32_t>((value_part ? kBarFullV : kBarFullS) + s);
+  const int nparts = value_part ? 4 : kChunks - 4;
+  mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox * nparts * rpb * 128));
+#pragma unroll 1
+  for (int k = 0; k < nbox; ++k) {
+    const int t = t0 + k * rpb;
+    // A block id outside [0, num_blocks) lands the box outside the cache
+    // tensor, where the copy reads zeros; the softmax warps flag the segment
+    // and zero its result.
+    const int row = bt[t >> p.log2_block_size] * bs + (t & (bs - 1));
+    const uint32_t off = static_cast<uint32_t>(k * rpb * 128);
+    if (rpb == kT) {
+      // One 64-row box per tile: a 3-D copy brings four chunks at once (this
+      // CTA's value chunks, or the other CTA's); chunk 8 (RoPE) goes with the
+      // score part.
+      const int c0 = value_part ? 4 * pr.rank : 4 - 4 * pr.rank;
+      tma_load_3d(st + (value_part ? kValueSlot : 0) * kCChunkBytes, pr.tm_c4, 0, row, c0, full);
+      if (!value_part) tma_load_2d(st + 4 * kCChunkBytes, pr.tm_c, 8 * kChunk, row, full);
+      continue;
+    }
+#pragma unroll 1
+    for (int c = 0; c < kChunks; ++c) {
+      const int pos = position_of(pr.rank, c);
+      if ((pos >= kValueSlot) != value_part) continue;
+      tma_load_2d(st + pos * kCChunkBytes + off, pr.tm_c, c * kChunk, row, full);
+    }
+  }
+  return true;
+}
+
+// Rank 0 pulls the tile at token t0 into L2 (whole-tile boxes only).
+__device__ __noinline__ void prefetch_tile(const Producer& pr, const int32_t* bt, int t0) {
+  const MlaParams& p = *pr.p;
+  const int id = bt[t0 >> p.log2_block_size];
+  if (id < 0 || id >= p.num_blocks) return;
+  const int row = id * p.block_size + (t0 & (p.block_size - 1));
+  tma_prefetch_l2_3d(pr.tm_c4, 0, row, 0);
+  tma_prefetch_l2_3d(pr.tm_c4, 0, row, 4);
+  tma_prefetch_l2_2d(pr.tm_c, 8 * kChunk, row);
+}
+
+// The score chain S = Q C(stage)^T over the 9 chunk positions: positions 0-4
+// (score chunks) take Q from TMEM, positions 5-8 (value chunks) from shared
+// memory.  `part` 0 issues positions 0-4 (the first MMA overwrites S), part 1
+// positions 5-8.  Fully unrolled: the issue rate of this single thread bounds
+// the chain.
+template <bool kBF16>
+__device__ __forceinline__ void issue_score_part(int part, uint32_t d, uint32_t tmem, uint64_t dq,
+                                                 uint64_t db) {
+  constexpr uint32_t idesc = idesc_f16(kBF16, 128, kT, false, false);
+  constexpr uint64_t kQChunkUnits = kQChunkBytes >> 4;
+  constexpr uint64_t kCChunkUnits = kCChunkBytes >> 4;
+  if (part == 0) {
+#pragma unroll
+    for (int pos = 0; pos < kValueSlot; ++pos)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc_mma_f16_ts(d, tmem + kTmemQ + pos * 32 + ks * 8, db + pos * kCChunkUnits + 2 * ks, idesc,
+                      (pos > 0 || ks > 0) ? 1u : 0u);
+  } else {
+#pragma unroll
+    for (int pos = kValueSlot; pos < kChunks; ++pos)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc_mma_f16(d, dq + (pos - kValueSlot) * kQChunkUnits + 2 * ks,
+                   db + pos * kCChunkUnits + 2 * ks, idesc, 1u);
+  }
 }
 
 template <bool kBF16>
@@ -253,11 +392,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), kSoftmaxThreads);
     mbar_init(bar(kBarQs), 1);
+    mbar_init(bar(kBarQFree), 1);
     mbar_init(bar(kBarSum), kSoftmaxThreads);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarKvFull + s), 2);
-      mbar_init(bar(kBarKvEmptyS + s), 1);
-      mbar_init(bar(kBarKvEmptyV + s), 1);
+      mbar_init(bar(kBarFullS + s), 1);
+      mbar_init(bar(kBarFullV + s), 1);
+      mbar_init(bar(kBarEmptyS + s), 1);
+      mbar_init(bar(kBarEmptyV + s), 1);
     }
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarSFree), kSoftmaxThreads);
@@ -265,12 +406,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarPvDone), 1);
     mbar_init(bar(kBarEpiW), kSoftmaxThreads);
     mbar_init(bar(kBarEpiR), 1);
-    mbar_init(bar(kBarEpiDone), 1);
-    mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrainS), 1);
+    mbar_init(bar(kBarDrainP), 1);
     *abort_word = 0;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMmaS) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -280,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     // ---------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_c);
@@ -293,163 +434,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int v_issued = 0;   // tiles whose value part is requested
       int q_issued = 0;   // segments whose Q part is requested
       bool ok = true;
-      // A stage holds all 9 column chunks of a tile.  This CTA's 4 value
-      // chunks (latent columns [256 r, 256 r + 256)) stay until PV(j); the
-      // other 5 are only read by S(j) and are refilled as soon as S(j) is
-      // done, so loads run ahead of the PV that would otherwise gate them.
-      auto load_part = [&](const int32_t* bt, int t_lo, int t_hi, int it, bool value_part) -> bool {
-        const int gi = g + it;
-        const int s = gi % kStages;
-        const uint32_t empty = bar((value_part ? kBarKvEmptyV : kBarKvEmptyS) + s);
-        if (!mbar_wait_or_abort(empty, ((gi / kStages) & 1) ^ 1, p.err_flag, abort_word))
-          return false;
-        const int t0 = t_lo + it * kT;
-        const int nval = min(kT, t_hi - t0);
-        const int nbox = (nval + rows_per_box - 1) / rows_per_box;
-        const uint32_t st = sbase + kOffRing + s * kStageBytes;
-        const int nparts = value_part ? 4 : kChunks - 4;
-        mbar_arrive_expect_tx(bar(kBarKvFull + s),
-                              static_cast<uint32_t>(nbox * nparts * rows_per_box * 128));
-        for (int k = 0; k < nbox; ++k) {
-          const int t = t0 + k * rows_per_box;
-          // A block id outside [0, num_blocks) lands the box outside the
-          // cache tensor, where the copy reads zeros; the softmax warps flag
-          // the segment and zero its result.
-          const int row = bt[t >> p.log2_block_size] * bs + (t & (bs - 1));
-          const uint32_t off = static_cast<uint32_t>(k * rows_per_box * 128);
-          // Default L2 policy: the peer CTA loads the same tile moments later.
-          if (rows_per_box == kT) {
-            // One 64-row box per tile: a 3-D copy brings four chunks at once
-            // (this CTA's value chunks, or the other CTA's), chunk 8 (RoPE)
-            // goes with the score part.
-            const int c0 = value_part ? 4 * static_cast<int>(rank) : 4 - 4 * static_cast<int>(rank);
-            tma_load_3d(st + c0 * kCChunkBytes, &tm_c4, 0, row, c0, bar(kBarKvFull + s));
-            if (!value_part)
-              tma_load_2d(st + 8 * kCChunkBytes, &tm_c, 8 * kChunk, row, bar(kBarKvFull + s));
-            continue;
-          }
-          for (int c = 0; c < kChunks; ++c) {
-            const bool is_value = (c >> 2) == static_cast<int>(rank) && c < 8;
-            if (is_value != value_part) continue;
-            tma_load_2d(st + c * kCChunkBytes + off, &tm_c, c * kChunk, row, bar(kBarKvFull + s));
-          }
-        }
-        if (value_part) v_issued = gi + 1; else s_issued = gi + 1;
+      Producer pr;
+      pr.p = &p;
+      pr.tm_c = &tm_c;
+      pr.tm_c4 = &tm_c4;
+      pr.abort = abort_word;
+      pr.ring = sbase + kOffRing;
+      pr.bar0 = bar0;
+      pr.rank = static_cast<int>(rank);
+      pr.rows_per_box = rows_per_box;
+      // A part's chunks are refilled once their last reader has completed
+      // (S(j - 2) for the score chunks, O += P(j - 2) C(j - 2) for the value
+      // chunks; for a segment's last tile, the epilogue staged there).
+      auto load = [&](const Seg& sg, const int32_t* bt, int it, bool value_part) -> bool {
+        const int t0 = sg.t0 + it * kT;
+        if (!load_part(pr, bt, t0, min(kT, sg.t1 - t0), g + it, value_part)) return false;
+        if (value_part) v_issued = g + it + 1; else s_issued = g + it + 1;
         return true;
       };
+      const bool do_prefetch = rank == 0 && rows_per_box == kT;
       Cursor cur = cur0;
       Seg sg;
       while (ok && next_seg(p, sc, cur, sg)) {
         if (sg.kind == kSegZero) continue;
         const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
+        const int32_t* bt = p.block_table + static_cast<size_t>(sg.b) * p.max_blocks_per_seq;
         // Q[:, 0:256) of this segment's sequence, once the previous
-        // segment's last S (tile g - 1, the last reader of the Q region) has
-        // completed: the previous epilogue stages its output in the ring, so
-        // this load overlaps it.
-        if (g > 0 && !mbar_wait_or_abort(bar(kBarKvEmptyS + (g - 1) % kStages),
-                                         ((g - 1) / kStages) & 1, p.err_flag, abort_word)) {
+        // segment's last S (the last reader of the Q region) has completed;
+        // this overlaps the previous segment's epilogue.
+        if (q_issued > 0 &&
+            !mbar_wait_or_abort(bar(kBarQFree), (q_issued - 1) & 1, p.err_flag, abort_word)) {
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(bar(kBarQs), kQSmemChunks * kQChunkBytes);
         for (int c = 0; c < kQSmemChunks; ++c)
-          tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_qa, c * kChunk, sg.b * kMlaHeads,
+          tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_qa, (4 * static_cast<int>(rank) + c) * kChunk, sg.b * kMlaHeads,
                       bar(kBarQs));
         ++q_issued;
-        // This segment's tiles, once the previous segment's epilogue has
-        // released the ring.
-        if (q_issued > 1 &&
-            !mbar_wait_or_abort(bar(kBarEpiDone), (q_issued - 2) & 1, p.err_flag, abort_word)) {
-          ok = false;
-          break;
-        }
-        const int32_t* bt = p.block_table + static_cast<size_t>(sg.b) * p.max_blocks_per_seq;
-        // The tensor pipe completes PV(j - 2) before S(j - 1), so the value
-        // part of tile j is requested before the score part of tile j + 1.
-        ok = load_part(bt, sg.t0, sg.t1, 0, false);
+        if (do_prefetch && n > 1) prefetch_tile(pr, bt, sg.t0 + kT);
+        // The value part of tile j is released by O += P(j - 2) C(j - 2),
+        // about when S(j - 1) completes and releases the score part of tile
+        // j + 1: request them in that order.
+        ok = load(sg, bt, 0, false);
         for (int it = 0; ok && it < n; ++it) {
-          ok = load_part(bt, sg.t0, sg.t1, it, true);
-          if (ok && it + 1 < n) ok = load_part(bt, sg.t0, sg.t1, it + 1, false);
+          if (do_prefetch && it + 2 < n) prefetch_tile(pr, bt, sg.t0 + (it + 2) * kT);
+          ok = load(sg, bt, it, true);
+          if (ok && it + 1 < n) ok = load(sg, bt, it + 1, false);
         }
         g += n;
       }
       // Wait for this thread's copies still in flight before the CTA may
       // exit, even when another thread has raised the abort word: a bulk
-      // copy must never land in the shared memory of a finished CTA.  A tile
-      // whose value part was never requested gets the missing arrival so
-      // that its phase completes once the score part has landed.  Each wait
-      // is bounded on its own.
-      if (v_issued < s_issued) mbar_arrive(bar(kBarKvFull + (s_issued - 1) % kStages));
+      // copy must never land in the shared memory of a finished CTA.  Each
+      // wait is bounded on its own.
       for (int it = max(0, s_issued - kStages); it < s_issued; ++it)
-        if (!mbar_wait(bar(kBarKvFull + it % kStages), (it / kStages) & 1, p.err_flag)) break;
+        if (!mbar_wait(bar(kBarFullS + it % kStages), (it / kStages) & 1, p.err_flag)) break;
+      for (int it = max(0, v_issued - kStages); it < v_issued; ++it)
+        if (!mbar_wait(bar(kBarFullV + it % kStages), (it / kStages) & 1, p.err_flag)) break;
       if (q_issued > 0) mbar_wait(bar(kBarQs), (q_issued - 1) & 1, p.err_flag);
     }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer (one thread)
+  } else if (warp == kWarpMmaS) {
+    // ---------------- score GEMM issuer (one thread)
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(kBF16, 128, kT, false, false);
-      constexpr uint32_t idesc_pv = idesc_f16(kBF16, 128, 256, false, true);
       // Shared-memory descriptors are built once; within a swizzle atom and
       // across chunks / stages only the 14-bit start address (16-byte units,
       // low bits of the descriptor) moves, so each MMA is one add + issue.
       const uint64_t dq = smem_desc_sw128(sbase + kOffQ, 16, 1024);
       const uint64_t dr = smem_desc_sw128(sbase + kOffRing, 16, 1024);
-      const uint64_t dv = smem_desc_sw128(
-          sbase + kOffRing + static_cast<uint32_t>(rank) * 4 * kCChunkBytes, kCChunkBytes, 1024);
       constexpr uint64_t kStageUnits = kStageBytes >> 4;
-      constexpr uint64_t kQChunkUnits = kQChunkBytes >> 4;
-      constexpr uint64_t kCChunkUnits = kCChunkBytes >> 4;
-      // S(i) = Q C(i)^T (M = 128 heads, N = 64 tokens, K = 576).  The S tile
-      // is reused: S(i) waits until the softmax has read S(i - 1).
-      auto issue_s = [&](int i) -> bool {
-        const int s = i % kStages;
-        if (!mbar_wait_or_abort(bar(kBarKvFull + s), (i / kStages) & 1, p.err_flag, abort_word))
-          return false;
-        if (i > 0 &&
-            !mbar_wait_or_abort(bar(kBarSFree), (i - 1) & 1, p.err_flag, abort_word))
-          return false;
-        tc_fence_after();
-        const uint64_t db = dr + static_cast<uint64_t>(s) * kStageUnits;
-        const uint32_t d = tmem + kTmemS;
-        // Fully unrolled: a rolled chunk loop measurably slows the issue of
-        // this 36-MMA chain (1.5 vs 1.2 us per tile on GB300).
-#pragma unroll
-        for (int c = 0; c < kQSmemChunks; ++c) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc_mma_f16(d, dq + c * kQChunkUnits + 2 * ks, db + c * kCChunkUnits + 2 * ks, idesc_s,
-                       (c > 0 || ks > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int c = kQSmemChunks; c < kChunks; ++c) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc_mma_f16_ts(d, tmem + kTmemQ + (c - kQSmemChunks) * 32 + ks * 8,
-                          db + c * kCChunkUnits + 2 * ks, idesc_s, 1u);
-        }
-        tc_commit(bar(kBarSFull));
-        tc_commit(bar(kBarKvEmptyS + s));
-        return true;
-      };
-      // O += P(j) C_lat(j) over this CTA's 256 value columns (MN-major B);
-      // the first tile of a segment overwrites O.
-      auto issue_pv = [&](int j, bool first) -> bool {
-        if (!mbar_wait_or_abort(bar(kBarPFull), j & 1, p.err_flag, abort_word)) return false;
-        tc_fence_after();
-        const uint64_t db = dv + static_cast<uint64_t>(j % kStages) * kStageUnits;
-#pragma unroll
-        for (int ks = 0; ks < kT / 16; ++ks)
-          tc_mma_f16_ts(tmem + kTmemO, tmem + kTmemP + ks * 8, db + ks * (2048 >> 4), idesc_pv,
-                        (!first || ks > 0) ? 1u : 0u);
-        tc_commit(bar(kBarPvDone));
-        tc_commit(bar(kBarKvEmptyV + j % kStages));
-        return true;
-      };
-      // Per segment: wait for its Q (TMEM part written by the softmax warps
-      // after the previous segment's epilogue, so O is free again), then
-      // S(j), PV(j), S(j + 1), ...  PV(j) goes before S(j + 1): the value
-      // chunks of tile j are released (and the load of tile j + 2 starts) as
-      // early as possible.
       bool ok = true;
       int g = 0, k = 0;
       Cursor cur = cur0;
@@ -457,26 +510,122 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (ok && next_seg(p, sc, cur, sg)) {
         if (sg.kind == kSegZero) continue;
         const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
+        // This segment's Q: the TMEM part (softmax warps) and the TMA part.
         ok = mbar_wait_or_abort(bar(kBarQ), k & 1, p.err_flag, abort_word) &&
              mbar_wait_or_abort(bar(kBarQs), k & 1, p.err_flag, abort_word);
-        for (int j = -1; ok && j < n; ++j) {  // j = -1 issues S(0) only
-          if (j >= 0) ok = issue_pv(g + j, j == 0);
-          if (ok && j + 1 < n) ok = issue_s(g + j + 1);
+        for (int j = 0; ok && j < n; ++j) {
+          const int gi = g + j;
+          const int s = gi % kStages;
+          const uint32_t ph = static_cast<uint32_t>(gi / kStages) & 1u;
+          // S is one TMEM tile: S(gi) waits until the softmax has read S(gi - 1).
+          if (gi > 0 && !mbar_wait_or_abort(bar(kBarSFree), (gi - 1) & 1, p.err_flag, abort_word)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_or_abort(bar(kBarFullS + s), ph, p.err_flag, abort_word)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t db = dr + static_cast<uint64_t>(s) * kStageUnits;
+          issue_score_part<kBF16>(0, tmem + kTmemS, tmem, dq, db);
+          if (!mbar_wait_or_abort(bar(kBarFullV + s), ph, p.err_flag, abort_word)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_score_part<kBF16>(1, tmem + kTmemS, tmem, dq, db);
+          tc_commit(bar(kBarSFull));
+          // A segment's last tile: its stage is released by the epilogue
+          // staged there; Q may be replaced once this S completes.
+          tc_commit(bar(j + 1 < n ? kBarEmptyS + s : kBarQFree));
         }
         g += n;
         ++k;
       }
       // Wait (bounded) until every MMA this thread issued has completed.
-      tc_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, p.err_flag);
+      tc_commit(bar(kBarDrainS));
+      mbar_wait(bar(kBarDrainS), 0, p.err_flag);
     }
-  } else {
+  } else if (warp == kWarpMmaPv) {
+    // ---------------- value GEMM issuer (one thread)
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_f16(kBF16, 128, 256, false, true);
+      const uint64_t dv =
+          smem_desc_sw128(sbase + kOffRing + kValueSlot * kCChunkBytes, kCChunkBytes, 1024);
+      constexpr uint64_t kStageUnits = kStageBytes >> 4;
+      bool ok = true;
+      int g = 0;
+      Cursor cur = cur0;
+      Seg sg;
+      while (ok && next_seg(p, sc, cur, sg)) {
+        if (sg.kind == kSegZero) continue;
+        const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
+        for (int j = 0; ok && j < n; ++j) {
+          const int gi = g + j;
+          if (!mbar_wait_or_abort(bar(kBarPFull), gi & 1, p.err_flag, abort_word)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // O += P(gi) C_lat(gi) over this CTA's 256 value columns (MN-major
+          // B); the first tile of a segment overwrites O.
+          const uint64_t db = dv + static_cast<uint64_t>(gi % kStages) * kStageUnits;
+#pragma unroll
+          for (int ks = 0; ks < kT / 16; ++ks)
+            tc_mma_f16_ts(tmem + kTmemO, tmem + kTmemP + ks * 8, db + ks * (2048 >> 4), idesc_pv,
+                          (j > 0 || ks > 0) ? 1u : 0u);
+          tc_commit(bar(kBarPvDone));
+          if (j + 1 < n) tc_commit(bar(kBarEmptyV + gi % kStages));
+        }
+        g += n;
+      }
+      tc_commit(bar(kBarDrainP));
+      mbar_wait(bar(kBarDrainP), 0, p.err_flag);
+    }
+  } else if (warp < kWarpProducer) {
     // ---------------- softmax warps: thread (h, ch) owns head h, column half ch
     const int h = (warp & 3) * 32 + lane;
     const int ch = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float* red_sum = reinterpret_cast<float*>(smem + kOffRed);       // [2 halves][128]
     const float scale = p.scale_log2;
+    // Q row h of sequence b at positions 0-4 (this CTA's score chunks) into
+    // TMEM (positions 5-8 arrive in shared memory by TMA); the two halves
+    // split the five 64-column chunks 3 + 2, all loads in flight before any
+    // store.  Called only while no MMA reads the Q columns (before the
+    // segment's first S, after the previous segment's last S has completed).
+    auto load_q_tmem = [&](int b) {
+      const size_t row = static_cast<size_t>(b) * kMlaHeads + h;
+      const uint4* qa = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_abs) +
+                                                       row * kMlaDc);
+      const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_rope) +
+                                                       row * kMlaDr);
+      const int p0 = ch == 0 ? 0 : 3, np = ch == 0 ? 3 : 2;
+      uint4 w[24];
+#pragma unroll
+      for (int kk = 0; kk < 24; ++kk) {
+        const int c = chunk_at(static_cast<int>(rank), p0 + kk / 8);
+        if (kk < np * 8) w[kk] = c < 8 ? qa[c * 8 + kk % 8] : qr[kk % 8];
+      }
+#pragma unroll
+      for (int cc = 0; cc < 3; ++cc) {
+        if (cc < np) {
+          float v[32];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            v[4 * kk] = __uint_as_float(w[cc * 8 + kk].x);
+            v[4 * kk + 1] = __uint_as_float(w[cc * 8 + kk].y);
+            v[4 * kk + 2] = __uint_as_float(w[cc * 8 + kk].z);
+            v[4 * kk + 3] = __uint_as_float(w[cc * 8 + kk].w);
+          }
+          tmem_st32(tmem + lane_base + kTmemQ + (p0 + cc) * 32, v);
+        }
+      }
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kBarQ));
+    };
     bool ok = true;
     int g = 0, k = 0, epi_round = 0;
     Cursor cur = cur0;
@@ -493,42 +642,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int n_tiles = (sg.t1 - sg.t0 + kT - 1) / kT;
       float m_used = kNegInf, l = 0.f;  // l: this half's partial row sum
+      // The first segment's Q; later segments' Q was loaded right after the
+      // previous segment's last tile.
+      if (k == 0) load_q_tmem(sg.b);
 
-      // Q row h, columns [256, 512) and the RoPE part, into TMEM (columns
-      // [0, 256) arrive in shared memory by TMA); the two halves split the
-      // five 64-column chunks 3 + 2, all loads in flight before any store.
-      // No MMA is in flight here: the previous segment's epilogue waited for
-      // its last PV, and this segment's first S waits for kBarQ.
-      {
-        const uint4* qa = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_abs) +
-                                                         (head0 + h) * kMlaDc) + 32;
-        const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_rope) +
-                                                         (head0 + h) * kMlaDr);
-        const int c0 = ch == 0 ? 0 : 3, nc = ch == 0 ? 3 : 2;
-        uint4 w[24];
-#pragma unroll
-        for (int kk = 0; kk < 24; ++kk) {
-          const int c = c0 + kk / 8;
-          if (kk < nc * 8) w[kk] = c < 4 ? qa[c * 8 + kk % 8] : qr[kk % 8];
-        }
-#pragma unroll
-        for (int cc = 0; cc < 3; ++cc) {
-          if (cc < nc) {
-            float v[32];
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              v[4 * kk] = __uint_as_float(w[cc * 8 + kk].x);
-              v[4 * kk + 1] = __uint_as_float(w[cc * 8 + kk].y);
-              v[4 * kk + 2] = __uint_as_float(w[cc * 8 + kk].z);
-              v[4 * kk + 3] = __uint_as_float(w[cc * 8 + kk].w);
-            }
-            tmem_st32(tmem + lane_base + kTmemQ + (c0 + cc) * 32, v);
-          }
-        }
-        tc_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(kBarQ));
-      }
       // Block ids of the segment (needed by the epilogue only, so checked
       // while the first tile is in flight): every warp checks all of them,
       // so the verdict is uniform without a CTA-wide barrier.
@@ -560,7 +677,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + kTmemS + (ch ^ 1) * 32, so);
         tc_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar(kBarSFree));  // the MMA thread may now compute S(j + 1)
+        mbar_arrive(bar(kBarSFree));  // the score issuer may now compute S(j + 1)
         // Tile max of the scaled scores over the row (masked columns ignored).
         const int nvo = nval - (ch ^ 1) * 32;  // valid columns of the partner half
         const float lowest = scale >= 0.f ? kNegInf : -kNegInf;
@@ -584,9 +701,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             so[kk] = scale >= 0.f ? fmaxf(so[kk], so[kk + w]) : fminf(so[kk], so[kk + w]);
         float mt = so[0] * scale;
         if (mt != mt) mt = kNegInf;  // an all-masked row (-inf * 0 cannot occur: scale != 0)
-        // P(j - 1) must have been consumed (and O updated) before P(j) is
-        // written or O is rescaled.  (The previous segment's last PV was
-        // waited for by its epilogue.)
+        // O += P(j - 1) C(j - 1) must have completed before P(j) is written
+        // or O is rescaled.  (The previous segment's last one was waited for
+        // by its epilogue.)
         if (j > 0 &&
             !mbar_wait_or_abort(bar(kBarPvDone), (gj - 1) & 1, p.err_flag, abort_word)) {
           ok = false;
@@ -627,7 +744,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               p1 = 2 * kk + 1 < nv ? p1 : 0.f;
             }
             ls[kk & 3] += p0 + p1;
-            pk[kk] = pack2<kBF16>(p0, p1);
+            // bf16 P without the pack conversion (see pack2_bf16_pos); fp16
+            // keeps cvt.rn, whose subnormal results an integer form would lose.
+            if constexpr (kBF16)
+              pk[kk] = pack2_bf16_pos(p0, p1);
+            else
+              pk[kk] = pack2<false>(p0, p1);
           }
           lt_tile = (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
@@ -635,8 +757,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_st16(tmem + lane_base + kTmemP + ch * 16, pk);
         if (nval < kT) {
           // Value rows past the sequence end may hold anything (even NaN): zero
-          // them so that P = 0 there contributes exactly nothing.
-          uint8_t* st = smem + kOffRing + (gj % kStages) * kStageBytes + rank * 4 * kCChunkBytes;
+          // them so that P = 0 there contributes exactly nothing.  S(j) has
+          // already read them; O += P(j) C(j) reads them after P(j) is published.
+          uint8_t* st = smem + kOffRing + (gj % kStages) * kStageBytes + kValueSlot * kCChunkBytes;
           const int t = ch * 128 + h;
           for (int e = t; e < (kT - nval) * 4 * 8; e += kSoftmaxThreads) {
             const int row = nval + e / 32, c = (e / 8) & 3, q = e & 7;
@@ -648,36 +771,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarPFull));
+        if (j + 2 == n_tiles) {
+          // Pull the next segment's Q rows into L2 for its TMEM load.
+          Cursor c2 = cur;
+          Seg nx;
+          bool have = false;
+          while (!have && next_seg(p, sc, c2, nx)) have = nx.kind != kSegZero;
+          if (have) {
+            const char* row = reinterpret_cast<const char*>(
+                static_cast<const uint16_t*>(p.q_abs) + (static_cast<size_t>(nx.b) * kMlaHeads + h) * kMlaDc);
+            for (int pos = ch == 0 ? 0 : 3; pos < (ch == 0 ? 3 : 5); ++pos) {
+              const int c = chunk_at(static_cast<int>(rank), pos);
+              if (c < 8)
+                prefetch_l2(row + c * 128);
+              else
+                prefetch_l2(static_cast<const uint16_t*>(p.q_rope) +
+                            (static_cast<size_t>(nx.b) * kMlaHeads + h) * kMlaDr);
+            }
+          }
+        }
       }
       if (!ok) break;
 
-      // Pull the next segment's Q row into L2 now; its TMEM load follows
-      // this epilogue on the critical path of the segment switch.
+      // The segment's last S has completed (it was read above): load the
+      // next segment's Q into TMEM now, so that its first S overlaps this
+      // epilogue.
       {
         Cursor c2 = cur;
         Seg nx;
         bool have = false;
         while (!have && next_seg(p, sc, c2, nx)) have = nx.kind != kSegZero;
-        if (have) {
-          const char* row = reinterpret_cast<const char*>(
-              static_cast<const uint16_t*>(p.q_abs) + (static_cast<size_t>(nx.b) * kMlaHeads + h) * kMlaDc);
-          if (ch == 0) {
-            prefetch_l2(row + 512);
-            prefetch_l2(row + 640);
-            prefetch_l2(row + 768);
-          } else {
-            prefetch_l2(row + 896);
-            prefetch_l2(static_cast<const uint16_t*>(p.q_rope) +
-                        (static_cast<size_t>(nx.b) * kMlaHeads + h) * kMlaDr);
-          }
-        }
+        if (have) load_q_tmem(nx.b);
       }
 
       // ---------------- epilogue: O row h, this thread's 128 columns, / l
+      const int g_last = g + n_tiles - 1;
       red_sum[ch * kMlaHeads + h] = l;
       mbar_arrive(bar(kBarSum));
       ok = mbar_wait_or_abort(bar(kBarSum), k & 1, p.err_flag, abort_word) &&
-           mbar_wait_or_abort(bar(kBarPvDone), (g + n_tiles - 1) & 1, p.err_flag, abort_word);
+           mbar_wait_or_abort(bar(kBarPvDone), g_last & 1, p.err_flag, abort_word);
       if (!ok) break;
       const float lt = l + red_sum[(ch ^ 1) * kMlaHeads + h];
       tc_fence_after();
@@ -688,21 +820,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         p.part_lse[static_cast<size_t>(slot) * kMlaHeads + h] =
             seg_bad ? DECATTN_POISON_LSE : (lt > 0.f ? m_used + lg2(lt) : kNegInf);
       // O / l leaves through shared memory and bulk tensor stores, staged in
-      // the cache ring (idle: every MMA of the segment has completed, and the
-      // producer requests the next segment's tiles only after kBarEpiDone):
-      // 128-row boxes of 128-byte rows, 128-byte swizzled (16-byte chunk j of
-      // row y at chunk j ^ (y % 8), conflict-free for a warp writing 32 rows).
-      // An fp32 partial (this CTA's 256 columns) is 8 boxes of 32 columns, a
-      // 16-bit output 4 boxes of 64; either way one round of bulk stores.
-      {
-        const int nbt = partial ? 4 : 2;  // boxes per thread
+      // the ring stage of the segment's last tile (idle: its S and O += P C
+      // have completed, and the producer refills it only after this
+      // epilogue releases it): 128-row boxes of 128-byte rows, 128-byte
+      // swizzled (16-byte chunk j of row y at chunk j ^ (y % 8),
+      // conflict-free for a warp writing 32 rows), four boxes per round.  A
+      // 16-bit output (this CTA's 256 columns) is 4 boxes of 64 columns, one
+      // round; an fp32 partial is 8 boxes of 32 columns, two rounds.
+      const uint32_t stage_off = static_cast<uint32_t>(kOffRing + (g_last % kStages) * kStageBytes);
+      const int rounds = partial ? 2 : 1;
 #pragma unroll 1
-        for (int cc = 0; cc < nbt; ++cc) {
-          uint8_t* box = smem + kOffRing + (ch * nbt + cc) * kQChunkBytes;
+      for (int rd = 0; ok && rd < rounds; ++rd) {
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          uint8_t* box = smem + stage_off + (ch * 2 + cc) * kQChunkBytes;
           uint4 v[8];
           if (partial) {
             float o[32];
-            tmem_ld32(tmem + lane_base + kTmemO + ch * 128 + cc * 32, o);
+            tmem_ld32(tmem + lane_base + kTmemO + ch * 128 + (rd * 2 + cc) * 32, o);
             tc_wait_ld();
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -732,12 +867,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) {
           ok = mbar_wait_or_abort(bar(kBarEpiW), epi_round & 1, p.err_flag, abort_word);
           if (ok) {
-            for (int bi = 0; bi < 2 * nbt; ++bi) {
-              const uint32_t src = sbase + kOffRing + bi * kQChunkBytes;
+            for (int sl = 0; sl < kEpiBoxes; ++sl) {
+              const uint32_t src = sbase + stage_off + sl * kQChunkBytes;
+              // staging slot sl = 2 ch + cc holds column box (ch, rd, cc)
               if (partial)
-                tma_store_2d(&tm_po, col0 + bi * 32, slot * kMlaHeads, src);
+                tma_store_2d(&tm_po, col0 + ((sl >> 1) * 4 + rd * 2 + (sl & 1)) * 32,
+                             slot * kMlaHeads, src);
               else
-                tma_store_2d(&tm_out, col0 + bi * 64, static_cast<int>(head0), src);
+                tma_store_2d(&tm_out, col0 + sl * 64, static_cast<int>(head0), src);
             }
             bulk_commit_group();
             bulk_wait_read_all();
@@ -748,10 +885,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++epi_round;
       }
       if (!ok) break;
-      if (threadIdx.x == 0) mbar_arrive(bar(kBarEpiDone));
-      // This thread's next segment writes Q into TMEM only now, after its
-      // own O reads; the MMA thread starts that segment (whose first PV
-      // overwrites O) only once all softmax threads have done so.
+      // The stage is free again: release both of its parts to the producer.
+      if (threadIdx.x == 0) {
+        mbar_arrive(bar(kBarEmptyS + g_last % kStages));
+        mbar_arrive(bar(kBarEmptyV + g_last % kStages));
+      }
       g += n_tiles;
       ++k;
     }
@@ -761,7 +899,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMmaS) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

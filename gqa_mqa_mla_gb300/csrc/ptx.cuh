@@ -110,14 +110,16 @@ DECATTN_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int* err_flag,
 }
 
 // Bounded wait that also gives up as soon as another thread of the CTA has
-// raised the shared abort word (after its own wait timed out).
-DECATTN_DEV bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, int* err_flag,
-                                    volatile int* abort, bool cluster_scope = false,
-                                    uint64_t limit_ns = kWaitTimeoutNs) {
+// raised the shared abort word (after its own wait timed out).  The polling
+// loop is kept out of line: kernels with many wait sites stay small, which
+// matters once several warps run different code on one SM (instruction-fetch
+// stalls); the first probe stays inline.
+static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint32_t bar, uint32_t parity, int* err_flag,
+                                                     volatile int* abort, bool cluster_scope,
+                                                     uint64_t limit_ns) {
   auto probe = [&]() {
     return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   };
-  if (probe()) return true;
   const uint64_t t0 = global_timer_ns();
   uint32_t spins = 0;
   while (!probe()) {
@@ -131,6 +133,13 @@ DECATTN_DEV bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, int* err_flag
     }
   }
   return true;
+}
+
+DECATTN_DEV bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, int* err_flag,
+                                    volatile int* abort, bool cluster_scope = false,
+                                    uint64_t limit_ns = kWaitTimeoutNs) {
+  if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_or_abort_slow(bar, parity, err_flag, abort, cluster_scope, limit_ns);
 }
 
 DECATTN_DEV bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* err_flag) {
@@ -184,6 +193,22 @@ DECATTN_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
+}
+
+// Bring a 3-D / 2-D box of a tensor into L2 ahead of its load (no shared
+// memory, no completion tracking).
+DECATTN_DEV void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+DECATTN_DEV void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 // 2-D tiled bulk tensor store shared -> global, tracked by this thread's bulk
@@ -277,6 +302,21 @@ DECATTN_DEV uint32_t pack2(float x, float y) {
   return w;
 }
 
+DECATTN_DEV uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Two non-negative finite floats to a packed bf16 pair (x in the low half),
+// rounded to nearest with ties away from zero, using integer adds and a byte
+// permute only.  On GB300 the float-to-16-bit pack conversions slow a
+// concurrent tcgen05.mma issuer on the same SM by up to ~1.8x; this form
+// does not.  Differs from cvt.rn (ties to even) only on exact ties.
+DECATTN_DEV uint32_t pack2_bf16_pos(float x, float y) {
+  return byte_perm(__float_as_uint(x) + 0x8000u, __float_as_uint(y) + 0x8000u, 0x7632u);
+}
+
 // Four e4m3 values packed in a word (byte 0 first) to two fp16x2 words:
 // lo = {byte 0, byte 1}, hi = {byte 2, byte 3}, the lower byte in the lower
 // half.
@@ -293,12 +333,6 @@ DECATTN_DEV uint32_t f32x2_to_e4m3x2(float x, float y) {
   uint16_t h;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(y), "f"(x));
   return h;
-}
-
-DECATTN_DEV uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
 }
 
 DECATTN_DEV uint32_t lds32(uint32_t addr) {
