@@ -23,14 +23,14 @@
 //
 // Tensor-core costs that shape the kernel (measured on GB300 with M = 128,
 // K = 16, bf16): one issuing thread cannot issue tcgen05.mma faster than one
-// per ~49 cycles (A in TMEM) or ~54 cycles (A in shared memory), whatever N
-// is up to 64, while the tensor pipe itself finishes an N = 64 MMA in 32
-// cycles (A in TMEM; 48 with A in shared memory, bound by shared-memory
-// bandwidth) and an N = 256 MMA in 128.  So the score chain (36 MMAs of
-// N = 64 per tile) is bound by its issue rate, and the value GEMM is issued
-// by a second thread: O += P(j) C_lat(j) runs on the tensor pipe while the
-// first thread issues S(j + 1), which itself runs while the softmax warps
-// work on tile j.
+// per ~36 cycles (A in TMEM) for any N up to 64 when the whole warp computes
+// the operands and one elected lane issues (about 50 cycles from a lane-0
+// branch, which needs three times the instructions per MMA); with A in
+// shared memory an N = 64 MMA takes 48 cycles (shared-memory bandwidth), an
+// N = 256 MMA 128.  So the score chain (36 MMAs of N = 64 per tile) is bound
+// by its issue rate, and the value GEMM is issued by a second warp:
+// O += P(j) C_lat(j) runs on the tensor pipe while the first warp issues
+// S(j + 1), which itself runs while the softmax warps work on tile j.
 //
 // Chunks: the 576 columns are nine 64-column chunks; CTA r's value chunks are
 // 4r..4r+3 (latent columns [256 r, 256 r + 256)), its score chunks the other
@@ -57,8 +57,8 @@
 //              both threads of a row read all 64 score columns and take
 //              the same row maximum, and keep separate partial row sums;
 //   warp 8     TMA producer for the cache ring, walking the block table;
-//   warp 9     TMEM allocator; one thread issues the score GEMMs;
-//   warp 10    one thread issues the value GEMMs.
+//   warp 9     TMEM allocator; issues the score GEMMs (one elected lane);
+//   warp 10    issues the value GEMMs (one elected lane).
 //
 // Ring: a stage holds all 9 column chunks of a 64-token tile.  This CTA's 4
 // value chunks (latent columns [256 r, 256 r + 256)) stay until O += P C
@@ -495,82 +495,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (q_issued > 0) mbar_wait(bar(kBarQs), (q_issued - 1) & 1, p.err_flag);
     }
   } else if (warp == kWarpMmaS) {
-    // ---------------- score GEMM issuer (one thread)
-    if (lane == 0) {
-      // Shared-memory descriptors are built once; within a swizzle atom and
-      // across chunks / stages only the 14-bit start address (16-byte units,
-      // low bits of the descriptor) moves, so each MMA is one add + issue.
-      const uint64_t dq = smem_desc_sw128(sbase + kOffQ, 16, 1024);
-      const uint64_t dr = smem_desc_sw128(sbase + kOffRing, 16, 1024);
-      constexpr uint64_t kStageUnits = kStageBytes >> 4;
-      bool ok = true;
-      int g = 0, k = 0;
-      Cursor cur = cur0;
-      Seg sg;
-      while (ok && next_seg(p, sc, cur, sg)) {
-        if (sg.kind == kSegZero) continue;
-        const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
-        // This segment's Q: the TMEM part (softmax warps) and the TMA part.
-        ok = mbar_wait_or_abort(bar(kBarQ), k & 1, p.err_flag, abort_word) &&
-             mbar_wait_or_abort(bar(kBarQs), k & 1, p.err_flag, abort_word);
-        for (int j = 0; ok && j < n; ++j) {
-          const int gi = g + j;
-          const int s = gi % kStages;
-          const uint32_t ph = static_cast<uint32_t>(gi / kStages) & 1u;
-          // S is one TMEM tile: S(gi) waits until the softmax has read S(gi - 1).
-          if (gi > 0 && !mbar_wait_or_abort(bar(kBarSFree), (gi - 1) & 1, p.err_flag, abort_word)) {
-            ok = false;
-            break;
-          }
-          if (!mbar_wait_or_abort(bar(kBarFullS + s), ph, p.err_flag, abort_word)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t db = dr + static_cast<uint64_t>(s) * kStageUnits;
-          issue_score_part<kBF16>(0, tmem + kTmemS, tmem, dq, db);
-          if (!mbar_wait_or_abort(bar(kBarFullV + s), ph, p.err_flag, abort_word)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+    // ---------------- score GEMM issuer: the whole warp runs the loop and
+    // computes the operands (uniform registers), lane 0 waits on the
+    // barriers and the elected lane (lane 0: the warp is converged) issues
+    // the MMAs and their commits.
+    // Shared-memory descriptors are built once; within a swizzle atom and
+    // across chunks / stages only the 14-bit start address (16-byte units,
+    // low bits of the descriptor) moves.
+    const uint64_t dq = smem_desc_sw128(sbase + kOffQ, 16, 1024);
+    const uint64_t dr = smem_desc_sw128(sbase + kOffRing, 16, 1024);
+    constexpr uint64_t kStageUnits = kStageBytes >> 4;
+    auto wait = [&](int b, uint32_t parity) -> bool {
+      bool w = true;
+      if (lane == 0) w = mbar_wait_or_abort(bar(b), parity, p.err_flag, abort_word);
+      return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+    };
+    bool ok = true;
+    int g = 0, k = 0;
+    Cursor cur = cur0;
+    Seg sg;
+    while (ok && next_seg(p, sc, cur, sg)) {
+      if (sg.kind == kSegZero) continue;
+      const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
+      // This segment's Q: the TMEM part (softmax warps) and the TMA part.
+      ok = wait(kBarQ, k & 1) && wait(kBarQs, k & 1);
+      for (int j = 0; ok && j < n; ++j) {
+        const int gi = g + j;
+        const int s = gi % kStages;
+        const uint32_t ph = static_cast<uint32_t>(gi / kStages) & 1u;
+        // S is one TMEM tile: S(gi) waits until the softmax has read S(gi - 1).
+        ok = (gi == 0 || wait(kBarSFree, (gi - 1) & 1)) && wait(kBarFullS + s, ph);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t db = dr + static_cast<uint64_t>(s) * kStageUnits;
+        if (elect_one()) issue_score_part<kBF16>(0, tmem + kTmemS, tmem, dq, db);
+        __syncwarp();
+        ok = wait(kBarFullV + s, ph);
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
           issue_score_part<kBF16>(1, tmem + kTmemS, tmem, dq, db);
           tc_commit(bar(kBarSFull));
-          // A segment's last tile: its stage is released by the epilogue
-          // staged there; Q may be replaced once this S completes.
+          // Q may be replaced once a segment's last S has completed.
           tc_commit(bar(j + 1 < n ? kBarEmptyS + s : kBarQFree));
         }
-        g += n;
-        ++k;
+        __syncwarp();
       }
-      // Wait (bounded) until every MMA this thread issued has completed.
+      g += n;
+      ++k;
+    }
+    // Wait (bounded) until every MMA this warp issued has completed.
+    if (elect_one()) {
       tc_commit(bar(kBarDrainS));
       mbar_wait(bar(kBarDrainS), 0, p.err_flag);
     }
+    __syncwarp();
   } else if (warp == kWarpMmaPv) {
-    // ---------------- value GEMM issuer (one thread)
-    if (lane == 0) {
-      constexpr uint32_t idesc_pv = idesc_f16(kBF16, 128, 256, false, true);
-      const uint64_t dv =
-          smem_desc_sw128(sbase + kOffRing + kValueSlot * kCChunkBytes, kCChunkBytes, 1024);
-      constexpr uint64_t kStageUnits = kStageBytes >> 4;
-      bool ok = true;
-      int g = 0;
-      Cursor cur = cur0;
-      Seg sg;
-      while (ok && next_seg(p, sc, cur, sg)) {
-        if (sg.kind == kSegZero) continue;
-        const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
-        for (int j = 0; ok && j < n; ++j) {
-          const int gi = g + j;
-          if (!mbar_wait_or_abort(bar(kBarPFull), gi & 1, p.err_flag, abort_word)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // O += P(gi) C_lat(gi) over this CTA's 256 value columns (MN-major
-          // B); the first tile of a segment overwrites O.
-          const uint64_t db = dv + static_cast<uint64_t>(gi % kStages) * kStageUnits;
+    // ---------------- value GEMM issuer (the same warp structure)
+    constexpr uint32_t idesc_pv = idesc_f16(kBF16, 128, 256, false, true);
+    const uint64_t dv =
+        smem_desc_sw128(sbase + kOffRing + kValueSlot * kCChunkBytes, kCChunkBytes, 1024);
+    constexpr uint64_t kStageUnits = kStageBytes >> 4;
+    bool ok = true;
+    int g = 0;
+    Cursor cur = cur0;
+    Seg sg;
+    while (ok && next_seg(p, sc, cur, sg)) {
+      if (sg.kind == kSegZero) continue;
+      const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
+      for (int j = 0; ok && j < n; ++j) {
+        const int gi = g + j;
+        bool w = true;
+        if (lane == 0) w = mbar_wait_or_abort(bar(kBarPFull), gi & 1, p.err_flag, abort_word);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        tc_fence_after();
+        // O += P(gi) C_lat(gi) over this CTA's 256 value columns (MN-major
+        // B); the first tile of a segment overwrites O.
+        const uint64_t db = dv + static_cast<uint64_t>(gi % kStages) * kStageUnits;
+        if (elect_one()) {
 #pragma unroll
           for (int ks = 0; ks < kT / 16; ++ks)
             tc_mma_f16_ts(tmem + kTmemO, tmem + kTmemP + ks * 8, db + ks * (2048 >> 4), idesc_pv,
@@ -578,11 +581,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_commit(bar(kBarPvDone));
           if (j + 1 < n) tc_commit(bar(kBarEmptyV + gi % kStages));
         }
-        g += n;
+        __syncwarp();
       }
+      g += n;
+    }
+    if (elect_one()) {
       tc_commit(bar(kBarDrainP));
       mbar_wait(bar(kBarDrainP), 0, p.err_flag);
     }
+    __syncwarp();
   } else if (warp < kWarpProducer) {
     // ---------------- softmax warps: thread (h, ch) owns head h, column half ch
     const int h = (warp & 3) * 32 + lane;

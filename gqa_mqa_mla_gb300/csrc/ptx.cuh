@@ -381,6 +381,19 @@ DECATTN_DEV void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, u
 
 // ------------------------------------------------------------------ cluster
 
+// Elects one lane of the converged warp (the lowest active one).  Issuing
+// tcgen05 instructions under this predicate, with the whole warp computing
+// the operands, lets them live in uniform registers: about a third of the
+// instructions per tcgen05.mma of a single-lane branch.
+DECATTN_DEV bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 l;\n\telect.sync l|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 DECATTN_DEV uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
