@@ -655,10 +655,13 @@ static int head_gemm_impl(const void* x, const void* w, void* y, int batch, int 
   const int b16 = (batch + 15) / 16 * 16;
   p.n_tile = b16 < 256 ? b16 : 256;
   if ((batch + p.n_tile - 1) / p.n_tile > 65535) return DECATTN_ERR_UNSUPPORTED;
-  // Enough ring stages to keep a CTA's whole K in flight where it fits: up
-  // to 8, within ~200 KB of shared memory.
+  // Ring stages: up to 8, within ~100 KB of shared memory, so that two CTAs
+  // fit an SM and a call launched right after this one (a programmatic
+  // dependent) can start streaming its weights while this one finishes
+  // (DeepSeek-V2 out GEMM, B = 32, 8 layers' weights in turn: 6.99 us with
+  // 8 stages and one CTA per SM).
   const int stage_bytes = 128 * 128 + p.n_tile * 128;
-  int stages = (200 * 1024) / stage_bytes;
+  int stages = (100 * 1024) / stage_bytes;
   stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
   p.stages = k / 64 < stages ? k / 64 : stages;
   p.tmem_cols = 32;

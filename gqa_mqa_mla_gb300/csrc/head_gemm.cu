@@ -18,6 +18,13 @@
 // with two bulk tensor stores.  Every wait is bounded; a timeout sets the
 // error flag, the CTA stops issuing, waits for its copies and MMAs in
 // flight, frees TMEM and writes nothing.
+//
+// The kernel is launched as a programmatic dependent of the previous kernel
+// on the stream: its CTAs may start while that kernel finishes.  The
+// weights do not depend on it, so the producer requests the first stages'
+// weight boxes at once and waits (griddepcontrol.wait) only before the
+// activation boxes; every global write follows that wait.  Each CTA lets the
+// next kernel start launching as soon as it runs.
 #include <mutex>
 
 #include "internal.h"
@@ -78,18 +85,30 @@ __global__ void __launch_bounds__(kGemmThreads, 4)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_w);
       tma_prefetch_desc(&tm_x);
       const int w_row = head * p.m + mt * 128;
+      // The first stages' weight boxes need nothing from the previous
+      // kernel; its activations (X) may, so they follow griddepcontrol.wait.
+      const int first = nk < S ? nk : S;
+      for (int c = 0; c < first; ++c) {
+        const uint32_t st = smem_u32(smem + c * stage_bytes);
+        mbar_arrive_expect_tx(full0 + 8 * c, static_cast<uint32_t>(stage_bytes));
+        tma_load_2d(st, &tm_w, c * kChunk, w_row, full0 + 8 * c);
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       int issued = 0;
       for (int c = 0; c < nk; ++c) {
         const int s = c % S;
-        if (!mbar_wait_or_abort(empty0 + 8 * s, ((c / S) & 1) ^ 1, p.err_flag, abort)) break;
         const uint32_t st = smem_u32(smem + s * stage_bytes);
-        mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(stage_bytes));
-        tma_load_2d(st, &tm_w, c * kChunk, w_row, full0 + 8 * s);
+        if (c >= first) {
+          if (!mbar_wait_or_abort(empty0 + 8 * s, ((c / S) & 1) ^ 1, p.err_flag, abort)) break;
+          mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(stage_bytes));
+          tma_load_2d(st, &tm_w, c * kChunk, w_row, full0 + 8 * s);
+        }
         tma_load_3d(st + kATileBytes, &tm_x, c * kChunk, head, n0, full0 + 8 * s);
         ++issued;
       }
@@ -203,11 +222,19 @@ cudaError_t launch_head_gemm(const HeadGemmParams& p, const CUtensorMap& tm_w,
   const dim3 grid(p.m / 128, p.heads, (p.batch + p.n_tile - 1) / p.n_tile);
   const cudaError_t e = bf16 ? allow_smem<true>() : allow_smem<false>();
   if (e != cudaSuccess) return e;
-  if (bf16)
-    head_gemm_kernel<true><<<grid, kGemmThreads, smem, stream>>>(tm_w, tm_x, tm_y, p);
-  else
-    head_gemm_kernel<false><<<grid, kGemmThreads, smem, stream>>>(tm_w, tm_x, tm_y, p);
-  return cudaGetLastError();
+  // Programmatic dependent launch (see the kernel's comment).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (bf16) return cudaLaunchKernelEx(&cfg, head_gemm_kernel<true>, tm_w, tm_x, tm_y, p);
+  return cudaLaunchKernelEx(&cfg, head_gemm_kernel<false>, tm_w, tm_x, tm_y, p);
 }
 
 }  // namespace decattn
