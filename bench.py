@@ -375,7 +375,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the separately timed 8-bit-cache GQA layer (not part of value)")
+                    help="skip the separately timed extras (not part of value)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the long-context and Llama-3.1-8B extras (small profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target wall time of the oracle CPU-baseline sample")
     ap.add_argument("--gqa-batch", type=int, default=None,
@@ -669,7 +671,7 @@ def main():
     # on its own.  Long context (B = 1 and 4 at S = 131072, inputs larger than
     # L2, back to back) and the Llama-3.1-8B-shaped MHA / GQA-8 / MQA sweep
     # (inputs of 671 / 168 / 21 MB, L2 flushed before every call).
-    if gx is not None and not args.no_extras:
+    if gx is not None and not args.no_extras and not args.no_sweep:
         extras = extras or {}
         nf = max(PART_MIN_CALLS, min(K, 500))
         for wl in ("long_ctx_b1_s128k", "long_ctx_b4_s128k"):
