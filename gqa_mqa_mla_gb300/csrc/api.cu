@@ -136,11 +136,12 @@ int window_span(int max_seq_len, int window, int block_size) {
 namespace {
 
 // Split count for `units` independent (sequence[, KV head]) work units on
-// `slots` resident CTAs, for the latency-bound 8-bit-cache kernel, which
-// gains from more CTAs in flight: one split per unit once there are 1.5
-// waves of CTAs; otherwise split each sequence until about two waves exist,
-// keeping at least two 64-token tiles per split (measured on the 70B-shaped
-// layer over an e4m3 cache: 2 splits 211 us, 1 split 233 us).
+// `slots` resident CTAs, for the latency-bound 8-bit-cache consumers of
+// wide groups, which gain from more CTAs in flight: one split per unit once
+// there are 1.5 waves of CTAs; otherwise split each sequence until about two
+// waves exist, keeping at least two 64-token tiles per split (measured on the
+// 70B-shaped layer with the 16-row padded consumer: 2 splits 211 us, 1 split
+// 233 us).
 int plan_splits(int units, int max_seq_len, int slots) {
   const int tiles = max_seq_len > 0 ? (max_seq_len + kTile - 1) / kTile : 1;
   if (units < 1) units = 1;
@@ -188,17 +189,18 @@ int plan_gqa_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms) 
 }
 
 int plan_gqa_fp8_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms) {
-  // The 8-bit-cache kernel for 2..16 query heads per KV head runs three CTAs
-  // per SM; the other consumers, two.  Below ~0.85 of a wave of units the
-  // one-wave rule holds here too (measured at S=131072: B=1, 48 splits
-  // 70.8 us / 114 splits 88.1; B=4, 12 splits 199 us / 29 splits 231); from
-  // there on the latency-bound kernel prefers about two waves (the 70B-shaped
-  // layer, 512 units on 456 slots: 2 splits 211 us, 1 split 233 us).
+  // Up to 8 query heads per KV head the 8-bit-cache kernel (transposed
+  // consumer, 95 registers, three 16 KB stages) runs four CTAs per SM and,
+  // like the 16-bit kernel, wants at most one wave (70B-shaped layer, 512
+  // units on 608 slots: 1 split 160 us, 2 splits 171, 4 splits 185; at
+  // B=16, 4 splits 48.4 us, 3 splits 50.0, 8 splits 55.6).  Wider groups run
+  // two CTAs per SM; from ~0.85 of a wave of units on, their latency-bound
+  // consumers prefer about two waves.
   const int group = h_kv > 0 ? h_q / h_kv : 1;
-  const int per_sm = (group >= 2 && group <= 16) ? 3 : 2;
+  const int per_sm = (group >= 2 && group <= 8) ? 4 : 2;
   const int slots = num_sms * per_sm;
   const int64_t units = static_cast<int64_t>(batch) * h_kv;
-  if (units * 100 < static_cast<int64_t>(slots) * 85)
+  if (per_sm == 4 || units * 100 < static_cast<int64_t>(slots) * 85)
     return plan_splits_one_wave(batch * h_kv, max_seq_len, slots);
   return plan_splits(batch * h_kv, max_seq_len, slots);
 }

@@ -36,7 +36,10 @@
 // 128-byte swizzle row holds a token's whole 128-d head, so a K or V tile is
 // [64 tokens][128 B].  The consumers build fp16 mma fragments straight from
 // those bytes (cvt e4m3x2 -> f16x2), with no staging copy; K's scale folds
-// into the score scale and V's into the output.
+// into the score scale and V's into the output.  Up to 16 query heads per KV
+// head they use the transposed products S^T = K Q^T, O^T += V^T P^T, where
+// the group is the mma's N and a group of 8 fills every tile
+// (MmaConsumerF8T); wider groups use the padded form (MmaConsumerF8).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -693,6 +696,197 @@ struct MmaConsumerF8 {
   __device__ __forceinline__ static int slot(int w, int r) { return w * kRowsPerWarp + (r & 15); }
 };
 
+// Tensor cores for 2..16 query heads per KV head over an 8-bit cache, in the
+// transposed form S^T = K Q^T and O^T += V^T P^T: a warp's 16 tokens are the
+// mma's M (scores) or its K (values) and the query group is its N, 8 heads
+// per n-tile.  A group of 8 then fills every mma -- half the mma work of the
+// 16-row padded form above, and half its accumulator registers, so more
+// warps fit an SM.  The conversions per cache byte are the same.
+//   Scores: ldmatrix gives a thread 4 consecutive head dims (4q .. 4q + 3)
+//   of token g = lane / 4 (or g + 8); they fill k-slots (2q, 2q+1) and
+//   (2q+8, 2q+9) of the A fragment, and Q^T's B fragments use the same dim
+//   order.  The result holds tokens (g, g + 8) x heads (2q, 2q + 1).
+//   Values: transposed ldmatrix plus a byte permute give the token pairs
+//   (2q, 2q + 1) of dims 2g and 2g + 1 of a 16-dim block: m-tile row g is dim
+//   2g, row g + 8 dim 2g + 1.  P^T's B fragment (tokens 2q, 2q+1 of head g) is
+//   the score layout transposed: movmatrix per 8 tokens.
+template <int NT, bool kBF16>
+struct MmaConsumerF8T {
+  static constexpr int kCacheBytes = 1;
+  static constexpr int kMinBlocks = NT == 1 ? 4 : 2;
+  static constexpr int kWarps = 4;
+  static constexpr int kRowsPerWarp = 8 * NT;
+
+  uint32_t qb[8][NT][2];  // Q^T B fragments: k-step, n-tile, dims (4q, 4q+1 | 4q+2, 4q+3)
+  float o[8][NT][4];      // O^T, 16-dim block b: (2g, 2q) (2g, 2q+1) (2g+1, 2q) (2g+1, 2q+1)
+  float m[NT][2], l[NT][2];
+  float v_scale;
+  int tok0, cw, lane;
+
+  __device__ __forceinline__ void init(const GqaParams& p, int b, int j, int cw_, int lane_) {
+    cw = cw_;
+    lane = lane_;
+    tok0 = cw * 16;
+    v_scale = p.v_scale[j];
+    const int G = p.group;
+    const int g = lane >> 2, q4 = lane & 3;
+    const uint16_t* qp = static_cast<const uint16_t*>(p.q);
+    const size_t base = (static_cast<size_t>(b) * p.h_q + static_cast<size_t>(j) * G) * kHeadDim;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = 8 * nt + g;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint2 w = make_uint2(0u, 0u);
+        if (h < G) w = *reinterpret_cast<const uint2*>(qp + base + h * kHeadDim + ks * 16 + 4 * q4);
+        const float2 f0 = unpack2<kBF16>(w.x), f1 = unpack2<kBF16>(w.y);
+        qb[ks][nt][0] = pack2<false>(f0.x, f0.y);
+        qb[ks][nt][1] = pack2<false>(f1.x, f1.y);
+      }
+      m[nt][0] = m[nt][1] = kNegInf;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb) o[bb][nt][0] = o[bb][nt][1] = o[bb][nt][2] = o[bb][nt][3] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void tile(uint8_t* stage, int nskip, int nval, float scale_log2) {
+    const unsigned span = static_cast<unsigned>(nval - nskip);  // nskip < nval
+    const int r0 = tok0;
+    if (r0 >= nval || r0 + 16 <= nskip) return;  // past the end, or before a sliding window
+    const uint32_t ks_base = smem_u32(stage);
+    const uint32_t vs_base = ks_base + kF8TileBytes;
+    if (r0 + 16 > nval || r0 < nskip) {
+      // Rows past the sequence end (or before a sliding window) may hold
+      // anything, even NaN codes; zero their V rows so that P = 0 there
+      // contributes exactly nothing.  Both ranges are under 16 rows.
+      uint8_t* vs = stage + kF8TileBytes;
+      const int lo = max(0, nskip - r0), hi = max(0, r0 + 16 - nval);
+      for (int idx = lane; idx < (lo + hi) * 8; idx += 32) {
+        const int k = idx >> 3;
+        const int r = k < lo ? r0 + k : nval + (k - lo);
+        *reinterpret_cast<uint4*>(vs + f8_off(r, idx & 7)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    const int g = lane >> 2;
+    const int mi = lane >> 3;
+    const int tok = r0 + ((mi & 1) << 3) + (lane & 7);
+    // S^T = K Q^T: one ldmatrix.x4 holds tokens 0-7 and 8-15 of k-steps 2w, 2w + 1.
+    float s[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t k0, k1, k2, k3;
+      ldsm_x4(ks_base + f8_off(tok, 2 * w + (mi >> 1)), k0, k1, k2, k3);
+      uint32_t a[4];
+      e4m3x4_to_f16x2(k0, a[0], a[2]);
+      e4m3x4_to_f16x2(k1, a[1], a[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816<false>(s[nt], a, qb[2 * w][nt][0], qb[2 * w][nt][1]);
+      e4m3x4_to_f16x2(k2, a[0], a[2]);
+      e4m3x4_to_f16x2(k3, a[1], a[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_16816<false>(s[nt], a, qb[2 * w + 1][nt][0], qb[2 * w + 1][nt][1]);
+    }
+    // Scale into the log2 domain and mask tokens outside [nskip, nval); ta,
+    // tb count from the window start (valid: [0, span)).
+    const int ta = r0 + g - nskip, tb = ta + 8;
+    const bool la = static_cast<unsigned>(ta) < span, lb = static_cast<unsigned>(tb) < span;
+    uint32_t pb[NT][2];
+    bool moved = false;
+    float cr[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      s[nt][0] = la ? s[nt][0] * scale_log2 : kNegInf;
+      s[nt][1] = la ? s[nt][1] * scale_log2 : kNegInf;
+      s[nt][2] = lb ? s[nt][2] * scale_log2 : kNegInf;
+      s[nt][3] = lb ? s[nt][3] * scale_log2 : kNegInf;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mx = fmaxf(s[nt][e], s[nt][e + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        // Every chunk holds at least one valid token, so the new maximum is finite.
+        const float mn = fmaxf(m[nt][e], mx);
+        cr[nt][e] = ex2(m[nt][e] - mn);
+        moved |= cr[nt][e] != 1.f;
+        m[nt][e] = mn;
+        l[nt][e] *= cr[nt][e];
+      }
+      const float p0 = ex2(s[nt][0] - m[nt][0]), p1 = ex2(s[nt][1] - m[nt][1]);
+      const float p2 = ex2(s[nt][2] - m[nt][0]), p3 = ex2(s[nt][3] - m[nt][1]);
+      l[nt][0] += p0 + p2;
+      l[nt][1] += p1 + p3;
+      pb[nt][0] = movmatrix_trans(pack2<false>(p0, p1));  // tokens 0-7
+      pb[nt][1] = movmatrix_trans(pack2<false>(p2, p3));  // tokens 8-15
+    }
+    // Rescale O only when some head's maximum moved (the factors are exactly
+    // 1 otherwise): after the first tiles that is rare.
+    if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          o[bb][nt][0] *= cr[nt][0]; o[bb][nt][1] *= cr[nt][1];
+          o[bb][nt][2] *= cr[nt][0]; o[bb][nt][3] *= cr[nt][1];
+        }
+      }
+    }
+    // O^T += V^T P^T: transposed ldmatrix per 16-dim block pair and token half.
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t v0, v1, v2, v3;  // (tokens 0-7, block 2w), (8-15, 2w), (0-7, 2w+1), (8-15, 2w+1)
+      ldsm_x4_trans(vs_base + f8_off(tok, 2 * w + (mi >> 1)), v0, v1, v2, v3);
+      uint32_t a[4];
+      e4m3x4_to_f16x2(byte_perm(v0, 0u, 0x3120u), a[0], a[1]);
+      e4m3x4_to_f16x2(byte_perm(v1, 0u, 0x3120u), a[2], a[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816<false>(o[2 * w][nt], a, pb[nt][0], pb[nt][1]);
+      e4m3x4_to_f16x2(byte_perm(v2, 0u, 0x3120u), a[0], a[1]);
+      e4m3x4_to_f16x2(byte_perm(v3, 0u, 0x3120u), a[2], a[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816<false>(o[2 * w + 1][nt], a, pb[nt][0], pb[nt][1]);
+    }
+  }
+
+  // Write this warp's (m, l, o) rows (query heads of the group) to the merge
+  // area; V's scale applies here.
+  __device__ __forceinline__ void finish(float* mo, float* mm, float* ml, int lane_) {
+    const int g = lane_ >> 2, q4 = lane_ & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        l[nt][e] += __shfl_xor_sync(0xffffffffu, l[nt][e], 4);
+        l[nt][e] += __shfl_xor_sync(0xffffffffu, l[nt][e], 8);
+        l[nt][e] += __shfl_xor_sync(0xffffffffu, l[nt][e], 16);
+      }
+      const int h0 = cw * kRowsPerWarp + 8 * nt + 2 * q4;
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb) {
+        const int d0 = 16 * bb + 2 * g;
+        *reinterpret_cast<float2*>(mo + h0 * kHeadDim + d0) =
+            make_float2(o[bb][nt][0] * v_scale, o[bb][nt][2] * v_scale);
+        *reinterpret_cast<float2*>(mo + (h0 + 1) * kHeadDim + d0) =
+            make_float2(o[bb][nt][1] * v_scale, o[bb][nt][3] * v_scale);
+      }
+      if (g == 0) {
+        mm[h0] = m[nt][0];
+        ml[h0] = l[nt][0];
+        mm[h0 + 1] = m[nt][1];
+        ml[h0 + 1] = l[nt][1];
+      }
+    }
+  }
+
+  __device__ __forceinline__ static bool covers(int /*w*/, int /*r*/) { return true; }
+  __device__ __forceinline__ static int slot(int w, int r) { return w * kRowsPerWarp + r; }
+};
+
 // ------------------------------------------------------------------ the kernel
 
 template <class Consumer>
@@ -943,7 +1137,9 @@ cudaError_t dispatch_fp8(const GqaParams& p, const CUtensorMap& tk, const CUtens
                          cudaStream_t stream) {
   constexpr int S = 4;  // 16 KB stages: keep as many cache bytes in flight as the 16-bit ring
   if (p.group == 1) return launch_one<CcConsumerF8<1, kBF16>, kBF16, S>(p, tk, tv, stream);
-  if (p.group <= 16) return launch_one<MmaConsumerF8<1, kBF16>, kBF16, S>(p, tk, tv, stream);
+  // Four CTAs per SM of the transposed consumer: three 16 KB stages each.
+  if (p.group <= 8) return launch_one<MmaConsumerF8T<1, kBF16>, kBF16, 3>(p, tk, tv, stream);
+  if (p.group <= 16) return launch_one<MmaConsumerF8T<2, kBF16>, kBF16, S>(p, tk, tv, stream);
   if (p.group <= 32) return launch_one<MmaConsumerF8<2, kBF16>, kBF16, S>(p, tk, tv, stream);
   return launch_one<MmaConsumerF8<4, kBF16>, kBF16, S>(p, tk, tv, stream);
 }

@@ -361,6 +361,14 @@ DECATTN_DEV void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32
                : "r"(addr));
 }
 
+// Transpose an 8x8 matrix of 16-bit elements held one word per lane (lane t:
+// row t / 4, columns 2 (t % 4) and 2 (t % 4) + 1) across the warp.
+DECATTN_DEV uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
 // D(16x8, f32) += A(16x16) * B(16x8), 16-bit inputs.
 template <bool kBF16>
 DECATTN_DEV void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {

@@ -84,6 +84,16 @@ def test_planner_is_bounded_and_spreads_long_sequences(lib):
     assert binding.mla_plan_splits(1, 65536, num_sms=152) >= 16
 
 
+def test_fp8_planner_fills_one_wave_of_four_ctas_per_sm_up_to_8_heads_per_kv_head(lib):
+    # 512 (sequence, KV head) units of the 70B-shaped layer fit the 608 slots
+    # of four CTAs per SM: one split; 128 units: four splits (0.84 of a wave).
+    assert binding.gqa_fp8_plan_splits(64, 64, 8, 8192, num_sms=152) == 1
+    assert binding.gqa_fp8_plan_splits(16, 64, 8, 8192, num_sms=152) == 4
+    # wider groups keep two CTAs per SM and about two waves
+    assert binding.gqa_fp8_plan_splits(64, 128, 8, 8192, num_sms=152) == 1
+    assert binding.gqa_fp8_plan_splits(16, 256, 8, 8192, num_sms=152) == 2
+
+
 def _launch(**kw):
     d = dict(batch=2, num_blocks=64, block_size=16, max_blocks_per_seq=16, max_seq_len=256,
              num_splits=1, dtype=binding.DECATTN_BF16, workspace=None, workspace_bytes=0,
