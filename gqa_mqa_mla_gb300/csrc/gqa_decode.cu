@@ -43,6 +43,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "gqa_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -924,31 +925,9 @@ __global__ void __launch_bounds__(32 * (1 + Consumer::kWarps), Consumer::kMinBlo
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
 
-  const int seq_len = p.seq_lens[b];
-  int bad = 0;
-  if (seq_len < 0 || seq_len > p.max_seq_len) {
-    bad = 1;
-    if (threadIdx.x == 0 && split == 0 && j == 0) flag_error(p.err_flag, kFlagBadSeqLen);
-  }
-  // A sliding window attends to tokens [w0, seq_len) ("07 · MHA/MQA/GQA/MLA
-  // quick learn": each token attends only to the last W tokens).  Tiles start
-  // at the block (or 64-token) boundary holding w0; blocks wholly before the
-  // window are never read.
-  const int w0 = (p.window > 0 && seq_len > p.window) ? seq_len - p.window : 0;
-  const int base = w0 & ~((p.block_size < kTile ? p.block_size : kTile) - 1);
-  const int t_begin = base + split * p.tokens_per_split;
-  const int t_end = bad ? t_begin : min(seq_len, t_begin + p.tokens_per_split);
-  if (!bad && t_end > t_begin) {
-    const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks_per_seq;
-    const int k1 = (t_end - 1) >> p.log2_block_size;
-    for (int k = (t_begin >> p.log2_block_size) + threadIdx.x; k <= k1; k += blockDim.x) {
-      const int id = bt[k];
-      if (id < 0 || id >= p.num_blocks) {
-        bad = 1;
-        flag_error(p.err_flag, kFlagBadBlock);
-      }
-    }
-  }
+  const GqaSpan span = gqa_span(p, split, j, b);
+  const int w0 = span.w0, t_begin = span.t_begin, t_end = span.t_end;
+  int bad = span.bad;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -962,16 +941,7 @@ __global__ void __launch_bounds__(32 * (1 + Consumer::kWarps), Consumer::kMinBlo
 
   const size_t row0 = static_cast<size_t>(b) * p.h_q + static_cast<size_t>(j) * G;
   if (bad || t_end <= t_begin) {
-    // Bad data: zeros plus the poison marker.  Empty range: zeros, lse = -inf.
-    for (int e = threadIdx.x; e < G * kHeadDim; e += blockDim.x) {
-      const int r = e / kHeadDim, d = e % kHeadDim;
-      if (p.n_split == 1) {
-        static_cast<uint16_t*>(p.out)[(row0 + r) * kHeadDim + d] = 0;
-      } else {
-        p.part_o[((row0 + r) * p.n_split + split) * kHeadDim + d] = 0.f;
-        if (d == 0) p.part_lse[(row0 + r) * p.n_split + split] = bad ? DECATTN_POISON_LSE : kNegInf;
-      }
-    }
+    gqa_write_empty(p, row0, G, split, bad);
     return;
   }
 
@@ -1117,6 +1087,9 @@ cudaError_t launch_one(const GqaParams& p, const CUtensorMap& tk, const CUtensor
   return cudaGetLastError();
 }
 
+// Groups wider than this run on the tcgen05 kernel (gqa_wide.cu).
+constexpr int kWideGroup = 16;
+
 template <bool kBF16>
 cudaError_t dispatch(const GqaParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                      cudaStream_t stream) {
@@ -1127,9 +1100,8 @@ cudaError_t dispatch(const GqaParams& p, const CUtensorMap& tk, const CUtensorMa
   // tensor cores against 2.2 TB/s for the warp-shuffle CUDA-core consumer,
   // which is issue- and latency-bound there).
   if (p.group == 1) return launch_one<CcConsumer<1, kBF16>, kBF16, S>(p, tk, tv, stream);
-  if (p.group <= 16) return launch_one<MmaConsumer<1, kBF16>, kBF16, S>(p, tk, tv, stream);
-  if (p.group <= 32) return launch_one<MmaConsumer<2, kBF16>, kBF16, S>(p, tk, tv, stream);
-  return launch_one<MmaConsumer<4, kBF16>, kBF16, S>(p, tk, tv, stream);
+  if (p.group <= kWideGroup) return launch_one<MmaConsumer<1, kBF16>, kBF16, S>(p, tk, tv, stream);
+  return launch_gqa_wide_partial(p, tk, tv, kBF16, stream);
 }
 
 template <bool kBF16>
