@@ -180,12 +180,11 @@ int plan_splits_one_wave(int units, int max_seq_len, int slots) {
 }  // namespace
 
 int plan_gqa_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms) {
-  // GQA partial kernel: two resident CTAs per SM (3-stage ring of 32 KB) up
-  // to 16 query heads per KV head; wider groups run 8 consumer warps and
-  // keep one CTA per SM.
-  const int group = h_kv > 0 ? h_q / h_kv : 1;
-  const int per_sm = group <= 16 ? 2 : 1;
-  return plan_splits_one_wave(batch * h_kv, max_seq_len, num_sms * per_sm);
+  // GQA partial kernels: two resident CTAs per SM, both the mma.sync one
+  // (3-stage ring of 32 KB, up to 16 query heads per KV head) and the
+  // tcgen05 one for wider groups (2-stage K and V rings, ~100 KB).
+  (void)h_q;
+  return plan_splits_one_wave(batch * h_kv, max_seq_len, num_sms * 2);
 }
 
 int plan_gqa_fp8_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms) {

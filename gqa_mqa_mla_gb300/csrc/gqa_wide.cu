@@ -26,7 +26,7 @@
 // An M = 64 MMA writes rows 0-15 to TMEM lanes 0-15, rows 16-31 to lanes
 // 32-47, rows 32-47 to 64-79 and rows 48-63 to 96-111.
 //
-// Warps (352 threads, one CTA per SM):
+// Warps (352 threads, two CTAs per SM):
 //   0-7  load Q; online softmax of S(j) into P(j); lazy O rescale; epilogue.
 //        Warp w reads TMEM lane quarter w % 4 (rows 16 (w % 4) .. + 15) with
 //        the 16x32bx2 shape: lanes t and t + 16 own row 16 (w % 4) + t, in
@@ -61,12 +61,17 @@ namespace decattn {
 namespace {
 
 constexpr int kM = 64;                            // query heads per CTA (MMA rows)
-constexpr int kStages = 4;                        // K / V ring depth
+// K / V ring depth: two stages keep a CTA at ~100 KB of shared memory, so
+// that two CTAs share an SM.  One CTA streams about 38 GB/s however deep
+// its ring (4 and 6 stages measured the same); two CTAs per SM reach the
+// copy rate (70B-shaped layer, 32 query heads per KV head, B = 64: 110.9 us
+// with one CTA per SM and 4 stages, 91.9 us with two and 2 stages).
+constexpr int kStages = 2;
 constexpr int kHalf = kTile * 128;                // one 64-column half of a tile: 8 KB
 constexpr int kKvTile = 2 * kHalf;                // a K or a V tile: 16 KB
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kStages * kKvTile;
-constexpr int kOffQ = kOffV + kStages * kKvTile;  // 128 KB
+constexpr int kOffQ = kOffV + kStages * kKvTile;  // 64 KB
 constexpr int kQBytes = 2 * kM * 128;             // 16 KB
 constexpr int kOffP = kOffQ + kQBytes;
 constexpr int kPBytes = kM * kTile * 2;           // 8 KB per buffer
