@@ -668,13 +668,15 @@ def main():
         del abs_, q_abs_out, o_out
 
     # ---------------- extras: the other 16-bit GQA workloads, each call timed
-    # on its own.  Long context (B = 1 and 4 at S = 131072, inputs larger than
-    # L2, back to back) and the Llama-3.1-8B-shaped MHA / GQA-8 / MQA sweep
+    # on its own.  Long context (B = 1 and 4 at S = 131072) and wide groups
+    # (32 and 64 query heads per KV head at S = 8192, the tensor-core path),
+    # inputs larger than L2, back to back; the Llama-3.1-8B-shaped MHA / GQA-8 / MQA sweep
     # (inputs of 671 / 168 / 21 MB, L2 flushed before every call).
     if gx is not None and not args.no_extras and not args.no_sweep:
         extras = extras or {}
         nf = max(PART_MIN_CALLS, min(K, 500))
-        for wl in ("long_ctx_b1_s128k", "long_ctx_b4_s128k"):
+        for wl in ("long_ctx_b1_s128k", "long_ctx_b4_s128k", "wide_g32_b64_s8k",
+                   "wide_g64_mqa_b128_s8k"):
             lx = synth.workload_inputs(wl, device=dev, seed=rank)
             l_ns = da.gqa_plan_splits(lx.batch, lx.h_q, lx.h_kv, lx.max_seq_len)
             l_ws = torch.empty(max(16, da.gqa_workspace_size(lx.batch, lx.h_q, l_ns)),
@@ -691,7 +693,8 @@ def main():
             l_gbps = lb / (l_ms * 1e-3) / 1e9
             extras[wl] = {"workload": wl, "GBps": l_gbps, "ms": l_ms, "steps_per_s": 1e3 / l_ms,
                           "bytes": lb, "calls_timed": nf, "frac_of_hbm_peak": l_gbps / hbm,
-                          "splits": l_ns, "l2": "inputs larger than L2, back to back"}
+                          "splits": l_ns, "l2": "inputs larger than L2, back to back",
+                          "query_heads_per_kv_head": lx.h_q // lx.h_kv}
             err |= int(flag.item())
             del lx, l_ws, l_out
         flush = torch.empty(320 << 20, dtype=torch.uint8, device=dev)

@@ -305,6 +305,13 @@ WORKLOADS = {
                                       dtype="bf16", table="permuted")),
     "long_ctx_b4_s128k": ("gqa", dict(batch=4, h_q=64, h_kv=8, seq_lens=131072, block_size=16,
                                       dtype="bf16", table="permuted")),
+    # wide query groups (tensor-core path): 32 query heads per KV head
+    # (70B-shaped heads on 2 KV heads) and 64 (MQA with 64 query heads)
+    "wide_g32_b64_s8k": ("gqa", dict(batch=64, h_q=64, h_kv=2, seq_lens=8192, block_size=16,
+                                     dtype="bf16", table="permuted", q_std=0.5)),
+    "wide_g64_mqa_b128_s8k": ("gqa", dict(batch=128, h_q=64, h_kv=1, seq_lens=8192,
+                                          block_size=16, dtype="bf16", table="permuted",
+                                          q_std=0.5)),
 }
 
 

@@ -172,3 +172,68 @@ def test_output_is_deterministic():
     a = _run(x)
     b = _run(x)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ---------------------------------------------------------------- wide groups
+# More than 16 query heads per KV head run on the tcgen05 kernel: ragged and
+# empty lengths, many splits (most of them empty for short sequences), bad
+# block ids and lengths.
+
+WIDE_LENS = [0, 1, 63, 64, 65, 700, 0, 4097, 130, 2000, 64 * 7 + 5, 3]
+
+
+@pytest.mark.parametrize("h_q,h_kv", [(32, 1), (64, 1), (64, 2), (48, 2), (40, 2), (68, 4)])
+@pytest.mark.parametrize("num_splits", [0, 2, 5, 64])
+def test_wide_groups_ragged_and_empty(h_q, h_kv, num_splits):
+    if h_q % h_kv or h_q // h_kv > 64:
+        pytest.skip("not a supported group")
+    x = synth.gqa_inputs(batch=len(WIDE_LENS), h_q=h_q, h_kv=h_kv, seq_lens=WIDE_LENS,
+                         block_size=16, dtype="bf16", seed=h_q + h_kv, device=DEV)
+    out = _run(x, num_splits)
+    rows = sample_rows(x.batch, x.h_q, None)
+    ref, _ = oracle_gqa(x, rows)
+    compare(gather_rows(out, rows), ref, f"wide h_q={h_q} h_kv={h_kv} splits={num_splits}")
+    # empty sequences: zero rows
+    for b, n in enumerate(WIDE_LENS):
+        if n == 0:
+            assert torch.all(out[b] == 0)
+
+
+@pytest.mark.parametrize("num_splits", [1, 3, 40])
+def test_wide_groups_bad_block_and_bad_length(num_splits):
+    lens = [300, 300, 300, 2000, 64]
+    x = synth.gqa_inputs(batch=5, h_q=64, h_kv=2, seq_lens=lens, block_size=16, dtype="bf16",
+                         seed=8, device=DEV)
+    bt = x.block_table.clone()
+    bt[1, 3] = x.num_blocks + 5  # out of range
+    sl = x.seq_lens.clone()
+    sl[4] = 10_000  # beyond max_seq_len
+    xb = synth.GQAInputs(**{**x.__dict__, "block_table": bt, "seq_lens": sl})
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(xb, num_splits, err_flag=flag)
+    assert int(flag.item()) & da.FLAG_BAD_BLOCK
+    assert int(flag.item()) & da.FLAG_BAD_SEQ_LEN
+    assert torch.all(out[1] == 0) and torch.all(out[4] == 0)
+    rows = np.array([[b, i] for b in (0, 2, 3) for i in range(64)], np.int32)
+    ref, _ = oracle_gqa(x, rows)
+    compare(gather_rows(out, rows), ref, "unaffected rows")
+
+
+def test_wide_groups_deterministic_for_every_split_count():
+    """Two calls give identical bits, and every split count matches the oracle."""
+    x = synth.gqa_inputs(batch=6, h_q=64, h_kv=1, seq_lens=("uniform", 1, 6000), block_size=16,
+                         dtype="bf16", seed=21, device=DEV)
+    rows = sample_rows(x.batch, x.h_q, 64)
+    ref, _ = oracle_gqa(x, rows)
+    for ns in (1, 2, 9, 64, 256):
+        o1 = _run(x, ns)
+        o2 = _run(x, ns)
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+        compare(gather_rows(o1, rows), ref, f"wide splits={ns}")
+
+
+@pytest.mark.parametrize("name", ["wide_g32_b64_s8k", "wide_g64_mqa_b128_s8k"])
+def test_wide_group_workloads_sampled(name):
+    """The bench's wide-group workloads at full size and planned splits."""
+    x = synth.workload_inputs(name, device=DEV)
+    _check(x, n_rows=64, what=name)
