@@ -314,8 +314,9 @@ def workload_config(parts, gx, mx) -> dict:
     return {
         "workload": f"{GQA_WORKLOAD} + {MLA_WORKLOAD}" if len(parts) > 1 else
         (GQA_WORKLOAD if parts == ["gqa"] else MLA_WORKLOAD),
-        "gqa": {"h_q": 64, "h_kv": 8, "d_head": 128, "batch": gx.batch, "seq_len": 8192,
-                "block_size": 16, "table": "permuted"} if gx is not None else None,
+        "gqa": {"h_q": gx.h_q, "h_kv": gx.h_kv, "d_head": gx.d_head, "batch": gx.batch,
+                "seq_len": gx.max_seq_len, "block_size": gx.block_size,
+                "table": "permuted"} if gx is not None else None,
         "mla": {"heads": 128, "d_c": 512, "d_rope": 64, "batch": mx.batch, "seq_len": 8192,
                 "block_size": 64, "table": "permuted"} if mx is not None else None,
         "l2": "inputs larger than L2 (no flush needed)", "parallelism": "replicas"}
@@ -384,7 +385,13 @@ def main():
                     help="override the GQA workload's batch (smaller cases for profiling)")
     ap.add_argument("--mla-batch", type=int, default=None,
                     help="override the MLA workload's batch (smaller cases for profiling)")
+    ap.add_argument("--gqa-workload", default=None,
+                    help="another 16-bit GQA workload of synth's table for the gqa part "
+                         "(profiling runs; the line's config names it)")
     args = ap.parse_args()
+    if args.gqa_workload:
+        global GQA_WORKLOAD
+        GQA_WORKLOAD = args.gqa_workload
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

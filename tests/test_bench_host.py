@@ -74,8 +74,9 @@ def test_mla_algorithmic_bytes_and_flops():
 def test_workload_config_is_the_workload_only():
     """Both arms print bench.workload_config: shapes, cache layout and the L2
     note of the measured workload, and no choice of the implementation."""
-    cfg = bench.workload_config(["gqa", "mla"],
-                                type("G", (), {"batch": 64})(), type("M", (), {"batch": 32})())
+    g = type("G", (), {"batch": 64, "h_q": 64, "h_kv": 8, "d_head": 128, "max_seq_len": 8192,
+                       "block_size": 16})()
+    cfg = bench.workload_config(["gqa", "mla"], g, type("M", (), {"batch": 32})())
     assert cfg["workload"] == f"{bench.GQA_WORKLOAD} + {bench.MLA_WORKLOAD}"
     assert cfg["gqa"] == {"h_q": 64, "h_kv": 8, "d_head": 128, "batch": 64, "seq_len": 8192,
                           "block_size": 16, "table": "permuted"}
