@@ -43,8 +43,8 @@ MLA_WORKLOAD = "deepseek_v2_mla_b32_s8k"
 GQA_FP8_WORKLOAD = "llama3_70b_b64_s8k_fp8"
 GQA_WINDOW = 4096  # sliding-window extra: the 70B-shaped layer attending to its last 4096 tokens
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GQA_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/gqa_decode.cu", "gqa_mqa_mla_gb300/csrc/ptx.cuh",
-                      "gqa_mqa_mla_gb300/csrc/internal.h"]
+GQA_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/gqa_decode.cu", "gqa_mqa_mla_gb300/csrc/gqa_common.cuh",
+                      "gqa_mqa_mla_gb300/csrc/ptx.cuh", "gqa_mqa_mla_gb300/csrc/internal.h"]
 MLA_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/mla_decode.cu", "gqa_mqa_mla_gb300/csrc/ptx.cuh",
                       "gqa_mqa_mla_gb300/csrc/internal.h"]
 GEMM_KERNEL_SOURCES = ["gqa_mqa_mla_gb300/csrc/head_gemm.cu", "gqa_mqa_mla_gb300/csrc/ptx.cuh",
