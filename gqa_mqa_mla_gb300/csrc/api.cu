@@ -192,14 +192,16 @@ int plan_gqa_fp8_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_s
   // consumer, 95 registers, three 16 KB stages) runs four CTAs per SM and,
   // like the 16-bit kernel, wants at most one wave (70B-shaped layer, 512
   // units on 608 slots: 1 split 160 us, 2 splits 171, 4 splits 185; at
-  // B=16, 4 splits 48.4 us, 3 splits 50.0, 8 splits 55.6).  Wider groups run
-  // two CTAs per SM; from ~0.85 of a wave of units on, their latency-bound
-  // consumers prefer about two waves.
+  // B=16, 4 splits 48.4 us, 3 splits 50.0, 8 splits 55.6).  Groups of 9..16
+  // run two CTAs per SM; from ~0.85 of a wave of units on, their
+  // latency-bound consumers prefer about two waves.  Wider groups go to the
+  // tensor-core kernel (two CTAs per SM), which, like its 16-bit form, wants
+  // one wave.
   const int group = h_kv > 0 ? h_q / h_kv : 1;
   const int per_sm = (group >= 2 && group <= 8) ? 4 : 2;
   const int slots = num_sms * per_sm;
   const int64_t units = static_cast<int64_t>(batch) * h_kv;
-  if (per_sm == 4 || units * 100 < static_cast<int64_t>(slots) * 85)
+  if (per_sm == 4 || group > 16 || units * 100 < static_cast<int64_t>(slots) * 85)
     return plan_splits_one_wave(batch * h_kv, max_seq_len, slots);
   return plan_splits(batch * h_kv, max_seq_len, slots);
 }

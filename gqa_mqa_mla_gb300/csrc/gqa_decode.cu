@@ -39,7 +39,7 @@
 // into the score scale and V's into the output.  Up to 16 query heads per KV
 // head they use the transposed products S^T = K Q^T, O^T += V^T P^T, where
 // the group is the mma's N and a group of 8 fills every tile
-// (MmaConsumerF8T); wider groups use the padded form (MmaConsumerF8).
+// (MmaConsumerF8T); wider groups go to the tcgen05 kernel of gqa_wide.cu.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -497,212 +497,12 @@ struct CcConsumerF8 {
   __device__ __forceinline__ static bool covers(int /*w*/, int /*r*/) { return true; }
 };
 
-// Tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation) for
-// G >= 2 over an 8-bit cache.  The tile is read with ldmatrix treating pairs
-// of bytes as 16-bit elements.
-//   Scores: ldmatrix gives a thread 4 consecutive head dims of one token,
-//   i.e. the fp16 pairs for k-slots (2q, 2q+1) and (2q+8, 2q+9) of the B
-//   fragment once the dims inside each 16-dim k-step are ordered
-//   (4q, 4q+1 | 4q+2, 4q+3) -> slots (2q, 2q+1 | 2q+8, 2q+9).  The query's A
-//   fragments use the same order, so every dot product is unchanged.
-//   Values: transposed ldmatrix gives a thread dims (2n, 2n+1) of the two
-//   tokens of its k-slot pair; a byte permute regroups them into the token
-//   pairs of dim 2n and of dim 2n+1.  So n-tile 2b + e, column n holds head
-//   dim 16b + 2n + e; finish() writes the dims back in order.
-template <int MT, bool kBF16>
-struct MmaConsumerF8 {
-  static constexpr int kCacheBytes = 1;
-  // Three CTAs per SM: the conversion chains need more warps in flight than
-  // the 16-bit path (whose tiles are twice the bytes per token).
-  static constexpr int kMinBlocks = MT == 1 ? 3 : 1;
-  static constexpr int kWarps = MT <= 4 ? 4 : MT;
-  static constexpr int kRowsPerWarp = 16;
-  static constexpr int kWarpsPerMtile = kWarps / MT;
-  static constexpr int kTokensPerWarp = kTile / kWarpsPerMtile;
-
-  uint32_t qa[8][4];  // fp16 A fragments of the padded query group (dim order above)
-  float o[16][4];     // n-tile 2b + e, column n: head dim 16b + 2n + e
-  float m[2], l[2];
-  float v_scale;
-  int mt, tok0, cw, lane;
-
-  __device__ __forceinline__ void init(const GqaParams& p, int b, int j, int cw_, int lane_) {
-    cw = cw_;
-    lane = lane_;
-    mt = cw % MT;
-    tok0 = (cw / MT) * kTokensPerWarp;
-    v_scale = p.v_scale[j];
-    const int G = p.group;
-    const int r_lo = mt * 16 + (lane >> 2);
-    const int r_hi = r_lo + 8;
-    const int q4 = lane & 3;
-    const uint16_t* qb = static_cast<const uint16_t*>(p.q);
-    const size_t base = (static_cast<size_t>(b) * p.h_q + static_cast<size_t>(j) * G) * kHeadDim;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int d0 = ks * 16 + 4 * q4;
-      uint2 lo = make_uint2(0u, 0u), hi = make_uint2(0u, 0u);
-      if (r_lo < G) lo = *reinterpret_cast<const uint2*>(qb + base + r_lo * kHeadDim + d0);
-      if (r_hi < G) hi = *reinterpret_cast<const uint2*>(qb + base + r_hi * kHeadDim + d0);
-      const float2 l0 = unpack2<kBF16>(lo.x), l1 = unpack2<kBF16>(lo.y);
-      const float2 h0 = unpack2<kBF16>(hi.x), h1 = unpack2<kBF16>(hi.y);
-      qa[ks][0] = pack2<false>(l0.x, l0.y);
-      qa[ks][1] = pack2<false>(h0.x, h0.y);
-      qa[ks][2] = pack2<false>(l1.x, l1.y);
-      qa[ks][3] = pack2<false>(h1.x, h1.y);
-    }
-#pragma unroll
-    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    m[0] = m[1] = kNegInf;
-    l[0] = l[1] = 0.f;
-  }
-
-  __device__ __forceinline__ void tile(uint8_t* stage, int nskip, int nval, float scale_log2) {
-    const unsigned span = static_cast<unsigned>(nval - nskip);  // nskip < nval
-    const uint32_t ks_base = smem_u32(stage);
-    const uint32_t vs_base = ks_base + kF8TileBytes;
-    const int q4 = lane & 3;
-#pragma unroll
-    for (int c = 0; c < kTokensPerWarp / 16; ++c) {
-      const int r0 = tok0 + 16 * c;
-      if (r0 >= nval) break;
-      if (r0 + 16 <= nskip) continue;  // wholly before a sliding window
-      if (r0 + 16 > nval || r0 < nskip) {
-        // Rows past the sequence end (or before a sliding window) may hold
-        // anything, even NaN codes; zero their V rows so that P = 0 there
-        // contributes exactly nothing.  Both ranges are under 16 rows.
-        uint8_t* vs = stage + kF8TileBytes;
-        const int lo = max(0, nskip - r0), hi = max(0, r0 + 16 - nval);
-        for (int idx = lane; idx < (lo + hi) * 8; idx += 32) {
-          const int k = idx >> 3;
-          const int r = k < lo ? r0 + k : nval + (k - lo);
-          *reinterpret_cast<uint4*>(vs + f8_off(r, idx & 7)) = make_uint4(0, 0, 0, 0);
-        }
-        __syncwarp();
-      }
-      // S = Q K^T for 16 tokens: two n-tiles of 8 tokens.  One ldmatrix.x4
-      // covers both token groups of k-steps 2w and 2w + 1.
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const int mi = lane >> 3;
-        const int tok = r0 + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint32_t k0, k1, k2, k3;  // (tokens 0-7, ks), (8-15, ks), (0-7, ks+1), (8-15, ks+1)
-          ldsm_x4(ks_base + f8_off(tok, 2 * w + (mi >> 1)), k0, k1, k2, k3);
-          uint32_t b0, b1, b2, b3;
-          e4m3x4_to_f16x2(k0, b0, b1);
-          e4m3x4_to_f16x2(k1, b2, b3);
-          mma_16816<false>(s0, qa[2 * w], b0, b1);
-          mma_16816<false>(s1, qa[2 * w], b2, b3);
-          e4m3x4_to_f16x2(k2, b0, b1);
-          e4m3x4_to_f16x2(k3, b2, b3);
-          mma_16816<false>(s0, qa[2 * w + 1], b0, b1);
-          mma_16816<false>(s1, qa[2 * w + 1], b2, b3);
-        }
-      }
-      // Scale into the log2 domain and mask tokens outside [nskip, nval).
-      // ta, tb count from the window start: valid rows are [0, span).
-      const int ta = r0 - nskip + 2 * q4, tb = ta + 8;
-      s0[0] = static_cast<unsigned>(ta) < span ? s0[0] * scale_log2 : kNegInf;
-      s0[1] = static_cast<unsigned>(ta + 1) < span ? s0[1] * scale_log2 : kNegInf;
-      s0[2] = static_cast<unsigned>(ta) < span ? s0[2] * scale_log2 : kNegInf;
-      s0[3] = static_cast<unsigned>(ta + 1) < span ? s0[3] * scale_log2 : kNegInf;
-      s1[0] = static_cast<unsigned>(tb) < span ? s1[0] * scale_log2 : kNegInf;
-      s1[1] = static_cast<unsigned>(tb + 1) < span ? s1[1] * scale_log2 : kNegInf;
-      s1[2] = static_cast<unsigned>(tb) < span ? s1[2] * scale_log2 : kNegInf;
-      s1[3] = static_cast<unsigned>(tb + 1) < span ? s1[3] * scale_log2 : kNegInf;
-      float mx_lo = fmaxf(fmaxf(s0[0], s0[1]), fmaxf(s1[0], s1[1]));
-      float mx_hi = fmaxf(fmaxf(s0[2], s0[3]), fmaxf(s1[2], s1[3]));
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-      // Every chunk holds at least one valid token, so the new maxima are finite.
-      const float mn_lo = fmaxf(m[0], mx_lo), mn_hi = fmaxf(m[1], mx_hi);
-      const float c_lo = ex2(m[0] - mn_lo), c_hi = ex2(m[1] - mn_hi);
-      m[0] = mn_lo;
-      m[1] = mn_hi;
-      l[0] *= c_lo;
-      l[1] *= c_hi;
-      // Rescale O only when some row's maximum moved (the factors are exactly
-      // 1 otherwise): after the first tiles that is rare.
-      if (__any_sync(0xffffffffu, c_lo != 1.f || c_hi != 1.f)) {
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          o[n][0] *= c_lo; o[n][1] *= c_lo; o[n][2] *= c_hi; o[n][3] *= c_hi;
-        }
-      }
-      const float p00 = ex2(s0[0] - mn_lo), p01 = ex2(s0[1] - mn_lo);
-      const float p02 = ex2(s0[2] - mn_hi), p03 = ex2(s0[3] - mn_hi);
-      const float p10 = ex2(s1[0] - mn_lo), p11 = ex2(s1[1] - mn_lo);
-      const float p12 = ex2(s1[2] - mn_hi), p13 = ex2(s1[3] - mn_hi);
-      l[0] += (p00 + p01) + (p10 + p11);
-      l[1] += (p02 + p03) + (p12 + p13);
-      const uint32_t pa[4] = {pack2<false>(p00, p01), pack2<false>(p02, p03),
-                              pack2<false>(p10, p11), pack2<false>(p12, p13)};
-      // O += P V: transposed ldmatrix per 16-dim block b and token half h
-      // gives {dims 2n, 2n+1} of tokens (2q, 2q+1) (+8 h); the permute makes
-      // the token pairs of dim 2n (low word) and dim 2n + 1 (high word).
-      {
-        const int mi = lane >> 3;
-        const int tok = r0 + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint32_t v0, v1, v2, v3;  // (tokens 0-7, block 2w), (8-15, 2w), (0-7, 2w+1), (8-15, 2w+1)
-          ldsm_x4_trans(vs_base + f8_off(tok, 2 * w + (mi >> 1)), v0, v1, v2, v3);
-          uint32_t a0, a1, c0, c1;
-          e4m3x4_to_f16x2(byte_perm(v0, 0u, 0x3120u), a0, a1);
-          e4m3x4_to_f16x2(byte_perm(v1, 0u, 0x3120u), c0, c1);
-          mma_16816<false>(o[4 * w], pa, a0, c0);
-          mma_16816<false>(o[4 * w + 1], pa, a1, c1);
-          e4m3x4_to_f16x2(byte_perm(v2, 0u, 0x3120u), a0, a1);
-          e4m3x4_to_f16x2(byte_perm(v3, 0u, 0x3120u), c0, c1);
-          mma_16816<false>(o[4 * w + 2], pa, a0, c0);
-          mma_16816<false>(o[4 * w + 3], pa, a1, c1);
-        }
-      }
-    }
-  }
-
-  __device__ __forceinline__ void finish(float* mo, float* mm, float* ml, int lane_) {
-    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
-    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
-    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
-    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
-    const int rl = lane_ >> 2, t4 = lane_ & 3;
-    float* lo = mo + (cw * kRowsPerWarp + rl) * kHeadDim;
-    float* hi = mo + (cw * kRowsPerWarp + rl + 8) * kHeadDim;
-#pragma unroll
-    for (int bb = 0; bb < 8; ++bb) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int n = 2 * bb + e;
-        const int d0 = 16 * bb + 4 * t4 + e, d1 = d0 + 2;  // columns 2 t4 and 2 t4 + 1
-        lo[d0] = o[n][0] * v_scale;
-        lo[d1] = o[n][1] * v_scale;
-        hi[d0] = o[n][2] * v_scale;
-        hi[d1] = o[n][3] * v_scale;
-      }
-    }
-    if (t4 == 0) {
-      mm[cw * kRowsPerWarp + rl] = m[0];
-      ml[cw * kRowsPerWarp + rl] = l[0];
-      mm[cw * kRowsPerWarp + rl + 8] = m[1];
-      ml[cw * kRowsPerWarp + rl + 8] = l[1];
-    }
-  }
-
-  __device__ __forceinline__ static bool covers(int w, int r) { return (w % MT) == (r >> 4); }
-  __device__ __forceinline__ static int slot(int w, int r) { return w * kRowsPerWarp + (r & 15); }
-};
-
 // Tensor cores for 2..16 query heads per KV head over an 8-bit cache, in the
 // transposed form S^T = K Q^T and O^T += V^T P^T: a warp's 16 tokens are the
 // mma's M (scores) or its K (values) and the query group is its N, 8 heads
-// per n-tile.  A group of 8 then fills every mma -- half the mma work of the
-// 16-row padded form above, and half its accumulator registers, so more
-// warps fit an SM.  The conversions per cache byte are the same.
+// per n-tile.  A group of 8 then fills every mma -- half the mma work of a
+// 16-row padded form (the query group as M), and half its accumulator
+// registers, so more warps fit an SM.
 //   Scores: ldmatrix gives a thread 4 consecutive head dims (4q .. 4q + 3)
 //   of token g = lane / 4 (or g + 8); they fill k-slots (2q, 2q+1) and
 //   (2q+8, 2q+9) of the A fragment, and Q^T's B fragments use the same dim
@@ -1111,9 +911,9 @@ cudaError_t dispatch_fp8(const GqaParams& p, const CUtensorMap& tk, const CUtens
   if (p.group == 1) return launch_one<CcConsumerF8<1, kBF16>, kBF16, S>(p, tk, tv, stream);
   // Four CTAs per SM of the transposed consumer: three 16 KB stages each.
   if (p.group <= 8) return launch_one<MmaConsumerF8T<1, kBF16>, kBF16, 3>(p, tk, tv, stream);
-  if (p.group <= 16) return launch_one<MmaConsumerF8T<2, kBF16>, kBF16, S>(p, tk, tv, stream);
-  if (p.group <= 32) return launch_one<MmaConsumerF8<2, kBF16>, kBF16, S>(p, tk, tv, stream);
-  return launch_one<MmaConsumerF8<4, kBF16>, kBF16, S>(p, tk, tv, stream);
+  if (p.group <= kWideGroup)
+    return launch_one<MmaConsumerF8T<2, kBF16>, kBF16, S>(p, tk, tv, stream);
+  return launch_gqa_wide_partial_fp8(p, tk, tv, kBF16, stream);
 }
 
 }  // namespace

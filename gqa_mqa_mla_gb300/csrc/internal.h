@@ -110,6 +110,9 @@ cudaError_t launch_gqa_partial(const GqaParams& p, const CUtensorMap& tm_k,
 // head) over a 16-bit cache; the same maps and outputs as launch_gqa_partial.
 cudaError_t launch_gqa_wide_partial(const GqaParams& p, const CUtensorMap& tm_k,
                                     const CUtensorMap& tm_v, bool bf16, cudaStream_t stream);
+// The same over an e4m3 cache (the 8-bit maps of launch_gqa_partial_fp8).
+cudaError_t launch_gqa_wide_partial_fp8(const GqaParams& p, const CUtensorMap& tm_k,
+                                        const CUtensorMap& tm_v, bool bf16, cudaStream_t stream);
 // tm_out: 16-bit [B * 128, 512] output, boxes of 64 x 128; tm_po: fp32
 // [2 n_pairs * 128, 512] partials, boxes of 32 x 128 (both 128-byte swizzle).
 // The same over an e4m3 KV cache (tm_k / tm_v: 8-bit maps, boxes of 128 B x

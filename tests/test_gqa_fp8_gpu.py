@@ -156,3 +156,66 @@ def test_fp8_path_matches_16bit_path_on_the_same_values():
                         x.seq_lens, scale=x.scale, max_seq_len=x.max_seq_len)
     o8 = _run(x)
     torch.testing.assert_close(o8.float(), o16.float(), rtol=2e-2, atol=1e-2)
+
+
+# Groups wider than 16 query heads per KV head run on the tensor-core kernel
+# that converts each landed e4m3 tile to f16 in shared memory.
+
+@pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("h_q,h_kv", [(64, 2), (40, 2), (64, 1)])
+def test_wide_groups_block_sizes_and_ragged_lengths(block_size, h_q, h_kv):
+    lens = [0, 1, 63, 64, 65, 257, 1000]
+    x = synth.gqa_fp8_inputs(batch=len(lens), h_q=h_q, h_kv=h_kv, seq_lens=lens,
+                             block_size=block_size, seed=block_size + h_q, device=DEV)
+    for ns in (1, 3, 0):
+        _check(x, ns, what=f"wide h_q={h_q} h_kv={h_kv} bs={block_size} splits={ns}")
+    assert torch.all(_run(x)[0] == 0), "seq_len 0 must give a zero row"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_wide_groups_nan_tails_and_sharp_softmax(dtype):
+    x = synth.gqa_fp8_inputs(batch=3, h_q=32, h_kv=1, seq_lens=[37, 100, 5], block_size=64,
+                             dtype=dtype, seed=13, tail="nan", device=DEV)
+    for ns in (1, 2):
+        _check(x, ns, what=f"wide nan tail {dtype}")
+    xs = synth.gqa_fp8_inputs(batch=2, h_q=64, h_kv=2, seq_lens=("uniform", 200, 3000),
+                              block_size=16, dtype=dtype, seed=14, q_std=4.0, device=DEV)
+    _check(xs, what=f"wide sharp {dtype}")
+
+
+@pytest.mark.parametrize("num_splits", [1, 3, 40])
+def test_wide_groups_bad_block_and_bad_length(num_splits):
+    x = synth.gqa_fp8_inputs(batch=5, h_q=64, h_kv=2, seq_lens=[300, 300, 300, 2000, 64],
+                             block_size=16, seed=8, device=DEV)
+    bt = x.block_table.clone()
+    bt[1, 3] = x.num_blocks + 5
+    sl = x.seq_lens.clone()
+    sl[4] = 10_000
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(x, num_splits, err_flag=flag, block_table=bt, seq_lens=sl)
+    assert int(flag.item()) & da.FLAG_BAD_BLOCK
+    assert int(flag.item()) & da.FLAG_BAD_SEQ_LEN
+    assert torch.all(out[1] == 0) and torch.all(out[4] == 0)
+    rows = np.array([[b, i] for b in (0, 2, 3) for i in range(64)], np.int32)
+    ref, _ = oracle_gqa_fp8(x, rows)
+    compare(gather_rows(out, rows), ref, "unaffected rows")
+
+
+def test_wide_groups_deterministic_for_every_split_count():
+    x = synth.gqa_fp8_inputs(batch=6, h_q=64, h_kv=1, seq_lens=("uniform", 1, 6000),
+                             block_size=16, seed=21, device=DEV)
+    rows = sample_rows(x.batch, x.h_q, 64)
+    ref, _ = oracle_gqa_fp8(x, rows)
+    for ns in (1, 2, 9, 64, 256):
+        o1 = _run(x, ns)
+        o2 = _run(x, ns)
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+        compare(gather_rows(o1, rows), ref, f"wide splits={ns}")
+
+
+@pytest.mark.parametrize("batch,h_q,h_kv", [(64, 64, 2), (128, 64, 1)])
+def test_wide_group_full_size_sampled(batch, h_q, h_kv):
+    """The wide-group shapes at 8K tokens per sequence and planned splits."""
+    x = synth.gqa_fp8_inputs(batch=batch, h_q=h_q, h_kv=h_kv, seq_lens=8192, block_size=16,
+                             seed=batch + h_kv, device=DEV)
+    _check(x, n_rows=64, what=f"wide fp8 b{batch} {h_q}/{h_kv} s8k")
