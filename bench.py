@@ -704,6 +704,30 @@ def main():
                           "query_heads_per_kv_head": lx.h_q // lx.h_kv}
             err |= int(flag.item())
             del lx, l_ws, l_out
+        # The MQA layer over an 8-bit cache (the tensor-core kernel's e4m3 mode).
+        wl = "wide_g64_mqa_b128_s8k_fp8"
+        ex = synth.workload_inputs(wl, device=dev, seed=rank)
+        e_ns = da.gqa_fp8_plan_splits(ex.batch, ex.h_q, ex.h_kv, ex.max_seq_len)
+        e_ws = torch.empty(max(16, da.gqa_workspace_size(ex.batch, ex.h_q, e_ns)),
+                           dtype=torch.uint8, device=dev)
+        e_out = torch.empty_like(ex.q)
+
+        def e_call():
+            da.gqa_decode_fp8kv(ex.q, ex.k_codes, ex.v_codes, ex.k_scale, ex.v_scale,
+                                ex.block_table, ex.seq_lens, scale=ex.scale,
+                                max_seq_len=ex.max_seq_len, out=e_out, num_splits=e_ns,
+                                workspace=e_ws, err_flag=flag)
+
+        e_ms = time_calls(e_call, nf, stream, dev)
+        eb = gqa_fp8_bytes(ex)
+        e_gbps = eb / (e_ms * 1e-3) / 1e9
+        extras[wl] = {"workload": wl, "GBps": e_gbps, "ms": e_ms, "steps_per_s": 1e3 / e_ms,
+                      "bytes": eb, "calls_timed": nf, "frac_of_hbm_peak": e_gbps / hbm,
+                      "splits": e_ns, "l2": "inputs larger than L2, back to back",
+                      "query_heads_per_kv_head": ex.h_q // ex.h_kv,
+                      "cache_dtype": "e4m3 (per-KV-head fp32 scales)"}
+        err |= int(flag.item())
+        del ex, e_ws, e_out
         flush = torch.empty(320 << 20, dtype=torch.uint8, device=dev)
         sweep = {}
         for wl in ("llama31_8b_mha_b16", "llama31_8b_gqa_b16", "llama31_8b_mqa_b16"):

@@ -312,6 +312,10 @@ WORKLOADS = {
     "wide_g64_mqa_b128_s8k": ("gqa", dict(batch=128, h_q=64, h_kv=1, seq_lens=8192,
                                           block_size=16, dtype="bf16", table="permuted",
                                           q_std=0.5)),
+    # the same MQA layer over an 8-bit (e4m3) KV cache
+    "wide_g64_mqa_b128_s8k_fp8": ("gqa_fp8", dict(batch=128, h_q=64, h_kv=1, seq_lens=8192,
+                                                  block_size=16, dtype="bf16",
+                                                  table="permuted", q_std=0.5)),
 }
 
 

@@ -213,9 +213,14 @@ def test_wide_groups_deterministic_for_every_split_count():
         compare(gather_rows(o1, rows), ref, f"wide splits={ns}")
 
 
-@pytest.mark.parametrize("batch,h_q,h_kv", [(64, 64, 2), (128, 64, 1)])
-def test_wide_group_full_size_sampled(batch, h_q, h_kv):
-    """The wide-group shapes at 8K tokens per sequence and planned splits."""
-    x = synth.gqa_fp8_inputs(batch=batch, h_q=h_q, h_kv=h_kv, seq_lens=8192, block_size=16,
-                             seed=batch + h_kv, device=DEV)
-    _check(x, n_rows=64, what=f"wide fp8 b{batch} {h_q}/{h_kv} s8k")
+def test_wide_group_full_size_sampled():
+    """32 query heads per KV head at B = 64, S = 8192, planned splits."""
+    x = synth.gqa_fp8_inputs(batch=64, h_q=64, h_kv=2, seq_lens=8192, block_size=16,
+                             seed=66, device=DEV)
+    _check(x, n_rows=64, what="wide fp8 b64 64/2 s8k")
+
+
+def test_wide_mqa_workload_sampled():
+    """The bench's MQA-64 workload over an e4m3 cache at full size."""
+    x = synth.workload_inputs("wide_g64_mqa_b128_s8k_fp8", device=DEV)
+    _check(x, n_rows=64, what="wide_g64_mqa_b128_s8k_fp8")
