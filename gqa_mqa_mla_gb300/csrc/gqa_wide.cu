@@ -48,13 +48,14 @@
 //
 // An 8-bit (e4m3) cache takes the same pipeline with three changes: the K
 // stage, as it lands, is the B operand of S = Q K^T on kind::f8f6f4, whose A
-// operand is Q split into three e4m3 terms (12 significant bits, scaled per
-// row by a power of two that the softmax undoes); the softmax threads
-// convert each landed V tile into a 16-bit slab (e4m3 -> f16 is exact) before
-// they publish P(j), the slab being the B operand of O += P V on f16; and the
-// rings hold three 8 KB stages.  A conversion warp of its own would put the
-// conversion (~1.3k cycles per 8 KB tile on one sub-partition) on the serial
-// path; spread over the eight softmax warps it is a few hundred cycles.
+// operand is Q split into e4m3 terms (two for a bf16 query, three for fp16:
+// exact, scaled per row by a power of two that the softmax undoes); the
+// softmax threads convert each landed V tile into one of two 16-bit slabs
+// (e4m3 -> f16 is exact) before they publish P(j), the slab being the B
+// operand of O += P V on f16; and the rings hold two 8 KB stages.  A
+// conversion warp of its own would put the conversion (~1.3k cycles per 8 KB
+// tile on one sub-partition) on the serial path; spread over the eight
+// softmax warps it is a few hundred cycles.
 //
 // Online softmax in the log2 domain with lazy rescaling, as the MLA kernel:
 // the running max used for the exponentials (and O in TMEM) moves only when
@@ -80,7 +81,7 @@ constexpr int kStages = 2;
 constexpr int kHalf = kTile * 128;                // one 64-column half of a tile: 8 KB
 constexpr int kKvTile = 2 * kHalf;                // a 16-bit K or V tile: 16 KB
 constexpr int kF8Tile = kTile * 128;              // an 8-bit K or V tile: 8 KB
-constexpr int kF8Stages = 3;                      // 8-bit K / V ring depth
+constexpr int kF8Stages = 2;                      // 8-bit K / V ring depth
 constexpr int kQBytes = 2 * kM * 128;             // 16 KB
 constexpr int kPBytes = kM * kTile * 2;           // 8 KB per buffer
 constexpr int kBarBytes = 256;
@@ -95,29 +96,31 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units: p stays <= 2^8
 
 // Shared-memory layout.  16-bit cache: K and V rings of 16-bit tiles (the
 // MMA operands), Q, two P buffers.  8-bit cache: K and V rings of 8-bit
-// tiles (the K stage is the score MMA's operand as it lands), one 16-bit V
-// slab (the softmax threads convert each landed V tile into it, f16, the
-// operand of O += P V), Q as three e4m3 terms, one P buffer — about 100 KB,
-// so that two CTAs still share an SM.
-constexpr int kQTerms = 3;                        // e4m3 terms of an 8-bit cache's Q
-constexpr int kQTermBytes = kM * 128;             // one term: [64 rows][128 codes]
-template <bool kF8>
+// tiles (the K stage is the score MMA's operand as it lands), two 16-bit V
+// slabs (the softmax threads convert each landed V tile into one, f16, the
+// operand of O += P V), Q as e4m3 terms, two P buffers — at most ~106 KB, so
+// that two CTAs still share an SM.
+constexpr int kQTermBytes = kM * 128;             // one e4m3 term of Q: [64 rows][128 codes]
+template <bool kBF16, bool kF8>
 struct WLayout {
   static constexpr int kRing = kF8 ? kF8Stages : kStages;
   static constexpr int kStageBytes = kF8 ? kF8Tile : kKvTile;
+  // e4m3 terms of an 8-bit cache's Q: a bf16 query (8 significant bits) is
+  // exactly two terms, an fp16 query (11) three.
+  static constexpr int kQTerms = kF8 ? (kBF16 ? 2 : 3) : 0;
   static constexpr int kOffK = 0;                                          // K ring
   static constexpr int kOffV = kOffK + kRing * kStageBytes;                // V ring
   static constexpr int kOffV16 = kOffV + kRing * kStageBytes;              // 8-bit: f16 V
-  static constexpr int kOffQ = kOffV16 + (kF8 ? kKvTile : 0);
-  static constexpr int kPBuffers = kF8 ? 1 : 2;
+  static constexpr int kOffQ = kOffV16 + (kF8 ? 2 * kKvTile : 0);
+  static constexpr int kPBuffers = 2;
   static constexpr int kOffP = kOffQ + (kF8 ? kQTerms * kQTermBytes : kQBytes);
   static constexpr int kOffBars = kOffP + kPBuffers * kPBytes;
   // Row sums of the two column groups, then (8-bit cache) 1 / alpha per row.
   static constexpr int kOffRed = kOffBars + kBarBytes;
   static constexpr int kSmemBytes = 1024 + kOffRed + 3 * kM * 4;
 };
-static_assert(WLayout<false>::kSmemBytes <= 232448 / 2 - 1024, "two 16-bit CTAs per SM");
-static_assert(WLayout<true>::kSmemBytes <= 232448 / 2 - 1024, "two 8-bit CTAs per SM");
+static_assert(WLayout<true, false>::kSmemBytes <= 232448 / 2 - 1024, "two 16-bit CTAs per SM");
+static_assert(WLayout<false, true>::kSmemBytes <= 232448 / 2 - 1024, "two 8-bit CTAs per SM");
 
 enum : int {
   kBarQ = 0,                        // Q in shared memory (256 arrivals)
@@ -211,7 +214,7 @@ __device__ __forceinline__ uint32_t e4m3_round2(float x, float y, float& rx, flo
 
 // kF8: the cache holds e4m3 codes with per-KV-head scales (K's folds into the
 // score scale, V's into the output).  S = Q K^T then runs as kind::f8f6f4 on
-// the landed K codes, with Q split into three e4m3 terms, and O += P V on f16
+// the landed K codes, with Q split into e4m3 terms, and O += P V on f16
 // operands (V converted by the softmax threads).
 template <bool kBF16, bool kF8>
 // (A minimum-blocks bound of 1 here made ptxas cap the registers at 168 and
@@ -219,7 +222,8 @@ template <bool kBF16, bool kF8>
 __global__ void __launch_bounds__(kThreads)
     gqa_wide_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const GqaParams p) {
-  using L = WLayout<kF8>;
+  using L = WLayout<kBF16, kF8>;
+  constexpr int kQTerms = L::kQTerms;
   constexpr bool kMmaBF16 = kBF16 && !kF8;  // operand type of O += P V (and 16-bit S)
   constexpr int kRing = L::kRing;
   extern __shared__ uint8_t smem_raw[];
@@ -382,9 +386,9 @@ __global__ void __launch_bounds__(kThreads)
     // its ring stage; 8-bit: the f16 slab, converted by the softmax threads
     // before they publish P(it).
     auto issue_pv = [&](int it) {
-      const int s = kF8 ? 0 : it % kRing;
+      const int s = it % kRing;  // 16-bit: the V ring stage; 8-bit: the f16 slab (it & 1)
       const uint64_t ap =
-          dp + static_cast<uint64_t>((((L::kPBuffers == 2 ? it : 0) & 1) * kPBytes) >> 4);
+          dp + static_cast<uint64_t>(((it & 1) * kPBytes) >> 4);
       const uint64_t bv = dv + static_cast<uint64_t>((s * kKvTile) >> 4);
       const uint32_t done = bar(kBarPvDone + (it & 1));
       const uint32_t acc0 = it > 0 ? 1u : 0u;
@@ -480,11 +484,13 @@ __global__ void __launch_bounds__(kThreads)
                                     (((c16 & 7) ^ (row & 7)) << 4)) = v;
         } else {
           // 8-bit cache: row r of Q times alpha_r = 2^k (the largest power of
-          // two with max |q_r| alpha_r <= 448) as the sum of three e4m3 terms
-          // t1 = e4m3(x), t2 = e4m3(x - t1), t3 = e4m3(x - t1 - t2): 12
-          // significant bits, so a 16-bit query is represented exactly except
-          // for parts below 2^-10 (e4m3's subnormal step) of the scaled row;
-          // the score row is scaled back by 1 / alpha_r.
+          // two with max |q_r| alpha_r <= 448) as the sum of e4m3 terms
+          // t1 = e4m3(x), t2 = e4m3(x - t1) (, t3 = e4m3(x - t1 - t2)): each
+          // residual is a multiple of the query's own last bit no larger than
+          // half of the previous term's, so two terms hold a bf16 query (8
+          // significant bits) and three an fp16 one (11) exactly, except for
+          // parts below 2^-10 (e4m3's subnormal step) of the scaled row; the
+          // score row is scaled back by 1 / alpha_r.
           float x[8];
           const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -625,8 +631,8 @@ __global__ void __launch_bounds__(kThreads)
         }
         l += ls[0] + ls[1];
       }
-      // P(it)'s buffer was last read by O += P(it - 2) V(it - 2) (two
-      // buffers) or O += P(it - 1) V(it - 1) (one).
+      // P(it)'s buffer (and, for an 8-bit cache, V(it)'s f16 slab) was last
+      // read by O += P(it - 2) V(it - 2).
       {
         const int last = it - L::kPBuffers;
         if (last >= 0 && !mbar_wait_or_abort(bar(kBarPvDone + (last & 1)), (last >> 1) & 1,
@@ -636,20 +642,21 @@ __global__ void __launch_bounds__(kThreads)
         }
       }
       if constexpr (kF8) {
-        // V(it) into the f16 slab (its last reader, O += P(it - 1) V(it - 1),
-        // has completed), then its 8-bit stage is free again.
+        // V(it) into f16 slab it % 2 (its last reader, O += P(it - 2) V(it - 2),
+        // has completed: the wait above), then its 8-bit stage is free again.
         const int s8 = it % kRing;
         if (!mbar_wait_or_abort(bar(kBarFullV + s8), (it / kRing) & 1, p.err_flag, abort_word)) {
           ok = false;
           break;
         }
-        convert_v8(smem + L::kOffV + s8 * kF8Tile, smem + L::kOffV16, threadIdx.x, nskip, nval);
+        convert_v8(smem + L::kOffV + s8 * kF8Tile, smem + L::kOffV16 + (it & 1) * kKvTile,
+                   threadIdx.x, nskip, nval);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarEmptyV + s8));
       }
       {
         // Row r, tokens c_own .. c_own + 15: 16-byte chunks c_own / 8 and + 1.
-        uint8_t* prow = smem + L::kOffP + ((L::kPBuffers == 2 ? it : 0) & 1) * kPBytes + r * 128;
+        uint8_t* prow = smem + L::kOffP + (it & 1) * kPBytes + r * 128;
         const int ch0 = c_own >> 3;
         *reinterpret_cast<uint4*>(prow + ((ch0 ^ (r & 7)) << 4)) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -732,7 +739,7 @@ template <bool kBF16, bool kF8>
 cudaError_t launch_t(const GqaParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                      cudaStream_t stream) {
   auto kern = gqa_wide_kernel<kBF16, kF8>;
-  constexpr int smem = WLayout<kF8>::kSmemBytes;
+  constexpr int smem = WLayout<kBF16, kF8>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_split, p.h_kv, p.batch);
