@@ -167,9 +167,14 @@ int gqa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
  *                     j is e4m3(code) * k_scale[j] (resp. v_scale[j])
  *   q, out            [batch, h_q, d_head] in launch->dtype (fp16 / bf16)
  * Every other argument, status and layout rule as gqa_decode (workspace
- * sized by gqa_decode_workspace_size).  Scores and P.V run on fp16 tensor-
- * core operands (the codes convert exactly; q is rounded to fp16) with fp32
- * accumulation; K's scale multiplies the scores, V's the output.
+ * sized by gqa_decode_workspace_size).  Scores and P.V run on tensor cores
+ * with fp32 accumulation; K's scale multiplies the scores, V's the output.
+ * Up to 16 query heads per KV head both take fp16 operands (the codes
+ * convert exactly; q is rounded to fp16).  From 17 on, the scores take the
+ * e4m3 codes as they are against q written as a sum of e4m3 terms (two for
+ * bf16, three for fp16, each row scaled by a power of two; exact except for
+ * parts below 2^-18 of the row's largest element), and P.V takes fp16
+ * operands.
  */
 int gqa_decode_fp8kv(const void* q, const void* k_cache, const void* v_cache,
                      const float* k_scale, const float* v_scale, const int32_t* block_table,
