@@ -39,9 +39,10 @@ struct GqaParams {
   const float* v_scale;           // [h_kv], 8-bit caches only
 };
 
-// MLA workspace (n_pairs > 1): a header of kHdrPref ints (tiles per pair,
-// total tiles), the first-tile index of every sequence (batch + 1 ints),
-// then the partial log2-sum-exps and outputs of 2 n_pairs slots.
+// MLA workspace (n_pairs > 1): a header of kHdrPref ints (slice width in
+// cost units, total tiles), the first-tile index of every sequence (batch + 1
+// ints), the first tile of every pair's slice (n_pairs + 1 ints), then the
+// partial log2-sum-exps and outputs of 2 n_pairs slots.
 constexpr int kHdrPref = 64;
 
 struct MlaParams {

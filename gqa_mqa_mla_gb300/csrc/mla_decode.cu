@@ -76,6 +76,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <climits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -137,19 +139,27 @@ static_assert(kEpiBoxes * kQChunkBytes <= kStageBytes, "epilogue staging must fi
 static_assert(kTmemP + kT / 2 <= kTmemCols, "tensor memory columns");
 
 // Work schedule.  The batch's 64-token tiles, sequence after sequence, form
-// one list of T_all tiles (an invalid seq_len counts as 0 tiles); pair p of
-// the P CTA pairs takes the slice [p T, p T + T), T = ceil(T_all / P), so
-// every pair streams the same number of tiles however ragged the lengths
-// are.  The slice is cut at sequence boundaries into segments: a segment
+// one list of T_all tiles (an invalid seq_len counts as 0 tiles).  A CTA
+// pair's time is its tiles plus a fixed cost for every sequence it starts
+// beyond its first (an epilogue, a new Q and a pipeline refill: about
+// kSegCost tiles' worth, measured with per-CTA clock stamps), so the list
+// is cut in cost units: tile g of the r-th non-empty sequence costs
+// position c(g) = g + kSegCost r, and pair p of the P pairs takes the tiles
+// with c(g) in [p W, p W + W), W = ceil(c_all / P).  A slice that would
+// start in the cost gap before a sequence starts at that sequence's first
+// tile.  The slice is cut at sequence boundaries into segments: a segment
 // holding a whole sequence writes its output rows directly; one holding
 // part of a sequence writes an fp32 partial (normalised O and log2-sum-exp)
 // that the combine merges.  Only a slice's first and last segments can be
 // partial; they go to workspace slots 2 p and 2 p + 1.  A sequence with no
-// tiles is zeroed by the pair whose slice contains its start.
+// tiles is zeroed by the pair whose slice contains its start (at tile
+// position t: the pair with lo <= t < the next pair's lo).
 enum : int { kSegZero = 0, kSegDirect = 1, kSegPartial = 2 };
+constexpr int kSegCost = 9;
 
 struct Sched {
-  int pair, n_pairs, T, lo, hi;  // this pair's tile slice [lo, hi)
+  int pair, n_pairs, lo, hi;  // this pair's tile slice [lo, hi)
+  int own_end;                // zero-length sequences at tile positions [lo, own_end) are ours
 };
 struct Cursor {
   int b, pref;  // next sequence to examine and the index of its first tile
@@ -185,10 +195,9 @@ __device__ __noinline__ bool next_seg(const MlaParams& p, const Sched& sc, Curso
     const int len = p.seq_lens[b];
     const int n = seq_tiles(p, len);
     if (n == 0) {
-      const int owner = min(pref / sc.T, sc.n_pairs - 1);
-      if (owner > sc.pair) return false;
+      if (pref >= sc.own_end) return false;  // a later pair's
       ++cur.b;
-      if (owner < sc.pair) continue;
+      if (pref < sc.lo) continue;            // an earlier pair's
       sg.b = b;
       sg.t0 = sg.t1 = 0;
       sg.kind = kSegZero;
@@ -321,52 +330,110 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col0 = static_cast<int>(rank) * 256;  // this CTA's O columns
 
-  // ---------------- schedule: block-wide scan of the per-sequence tile counts
+  // ---------------- schedule: block-wide scan of the per-sequence tile
+  // counts and non-empty-sequence counts
   Sched sc;
   sc.pair = static_cast<int>(blockIdx.x >> 1);
   sc.n_pairs = static_cast<int>(gridDim.x >> 1);
   Cursor cur0;
   {
-    int* s_warp = reinterpret_cast<int*>(smem + kOffRed);  // [0, 32) totals, [32, 64) scanned
-    int* s_misc = s_warp + 64;                              // b_start, its first tile
+    // [0, 32) / [32, 64): per-warp totals / scanned totals of tiles;
+    // [64, 96) / [96, 128): the same for non-empty sequences
+    int* s_warp = reinterpret_cast<int*>(smem + kOffRed);
+    int* s_misc = s_warp + 128;  // cursor sequence, its first tile, lo, hi
     constexpr int kWarpsAll = kThreads / 32;
     const int chunk = (p.batch + kThreads - 1) / kThreads;
     const int b_a = min(p.batch, static_cast<int>(threadIdx.x) * chunk);
     const int b_b = min(p.batch, b_a + chunk);
-    int sum = 0;
+    int sum = 0, cnt = 0;
     bool bad_len = false;
     for (int b = b_a; b < b_b; ++b) {
       const int len = p.seq_lens[b];
       bad_len |= (len < 0 || len > p.max_seq_len);
-      sum += seq_tiles(p, len);
+      const int n = seq_tiles(p, len);
+      sum += n;
+      cnt += n > 0;
     }
     if (bad_len && sc.pair == 0 && rank == 0) flag_error(p.err_flag, kFlagBadSeqLen);
-    int x = sum;
+    int x = sum, y = cnt;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, off);
-      if (lane >= off) x += y;
+      const int xu = __shfl_up_sync(0xffffffffu, x, off);
+      const int yu = __shfl_up_sync(0xffffffffu, y, off);
+      if (lane >= off) {
+        x += xu;
+        y += yu;
+      }
     }
-    if (lane == 31) s_warp[warp] = x;
-    if (threadIdx.x == 0) s_misc[0] = p.batch;
+    if (lane == 31) {
+      s_warp[warp] = x;
+      s_warp[64 + warp] = y;
+    }
     __syncthreads();
     if (warp == 0) {
       int v = lane < kWarpsAll ? s_warp[lane] : 0;
+      int u = lane < kWarpsAll ? s_warp[64 + lane] : 0;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += y;
+        const int vu = __shfl_up_sync(0xffffffffu, v, off);
+        const int uu = __shfl_up_sync(0xffffffffu, u, off);
+        if (lane >= off) {
+          v += vu;
+          u += uu;
+        }
       }
       s_warp[32 + lane] = v;
+      s_warp[96 + lane] = u;
     }
     __syncthreads();
     const int t_all = s_warp[32 + kWarpsAll - 1];
-    sc.T = max(1, (t_all + sc.n_pairs - 1) / sc.n_pairs);
-    sc.lo = sc.pair * sc.T;
-    sc.hi = min(sc.lo + sc.T, t_all);
+    const int ne_all = s_warp[96 + kWarpsAll - 1];
+    const int64_t c_all = t_all + static_cast<int64_t>(kSegCost) * max(0, ne_all - 1);
+    const int64_t W0 = (c_all + sc.n_pairs - 1) / sc.n_pairs;
+    const int64_t W = W0 > 1 ? W0 : 1;
+    const int excl_t = (warp > 0 ? s_warp[32 + warp - 1] : 0) + x - sum;
+    const int excl_r = (warp > 0 ? s_warp[96 + warp - 1] : 0) + y - cnt;
+    // Slice starts: the pair whose cost target p W falls on tile g of a
+    // sequence starts there; a target in the gap before a sequence starts
+    // at its first tile; targets past the last tile start at t_all.
+    int* starts = p.ws_hdr ? p.ws_hdr + kHdrPref + p.batch + 1 : nullptr;  // [n_pairs + 1]
+    const bool table = starts && sc.pair == 0 && rank == 0;
+    if (threadIdx.x == 0) {
+      s_misc[2] = t_all;
+      s_misc[3] = t_all;
+    }
+    if (table)
+      for (int q = threadIdx.x; q <= sc.n_pairs; q += kThreads) starts[q] = t_all;
+    __syncthreads();
+    {
+      int pref = excl_t, r = excl_r;
+      const int64_t lo_c = sc.pair * W, hi_c = lo_c + W;
+      for (int b = b_a; b < b_b; ++b) {
+        const int n = seq_tiles(p, p.seq_lens[b]);
+        if (n > 0) {
+          const int64_t cpref = pref + static_cast<int64_t>(kSegCost) * r;
+          const int64_t prev_end = r == 0 ? -1 : cpref - kSegCost - 1;  // previous sequence's last tile
+          const int64_t last = cpref + n - 1;
+          // tile of this sequence where cost target c starts (c in (prev_end, last])
+          auto at = [&](int64_t c) { return pref + static_cast<int>(c > cpref ? c - cpref : 0); };
+          if (lo_c > prev_end && lo_c <= last) s_misc[2] = at(lo_c);
+          if (hi_c > prev_end && hi_c <= last) s_misc[3] = at(hi_c);
+          if (table)
+            for (int64_t q = prev_end < 0 ? 0 : prev_end / W + 1; q <= last / W && q <= sc.n_pairs;
+                 ++q)
+              starts[q] = at(q * W);
+          ++r;
+        }
+        pref += n;
+      }
+    }
+    if (threadIdx.x == 0) s_misc[0] = p.batch;
+    __syncthreads();
+    sc.lo = s_misc[2];
+    sc.hi = sc.pair + 1 < sc.n_pairs ? s_misc[3] : t_all;
+    sc.own_end = sc.pair + 1 < sc.n_pairs ? sc.hi : INT_MAX;
     // First sequence this pair touches: pref_b + max(n_b, 1) > lo.
-    const int excl = (warp > 0 ? s_warp[32 + warp - 1] : 0) + x - sum;
-    int pref = excl, cand = p.batch, cand_pref = 0;
+    int pref = excl_t, cand = p.batch, cand_pref = 0;
     for (int b = b_a; b < b_b; ++b) {
       const int n = seq_tiles(p, p.seq_lens[b]);
       if (cand == p.batch && pref + max(n, 1) > sc.lo) {
@@ -378,7 +445,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (cand < p.batch) atomicMin(&s_misc[0], cand);
     if (p.ws_hdr && sc.pair == 0 && rank == 0 && threadIdx.x == 0) {
-      p.ws_hdr[0] = sc.T;
+      p.ws_hdr[0] = static_cast<int>(W);
       p.ws_hdr[1] = t_all;
       p.ws_hdr[kHdrPref + p.batch] = t_all;
     }
