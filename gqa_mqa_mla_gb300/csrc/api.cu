@@ -225,9 +225,10 @@ size_t mla_workspace_bytes(int batch, int n_pairs, size_t* off_lse, size_t* off_
   if (batch < 1 || n_pairs < 1 || n_pairs > DECATTN_MAX_SPLITS) return 0;
   if (n_pairs == 1) return 0;
   const size_t slots = 2 * static_cast<size_t>(n_pairs);
-  // header, per-sequence first tiles (batch + 1), pair slice starts (n_pairs + 1)
+  // header, per-sequence first tiles (batch + 1), pair slice starts (n_pairs + 1),
+  // per-sequence first cost positions (batch)
   const size_t hdr =
-      align_up((static_cast<size_t>(kHdrPref) + batch + 1 + n_pairs + 1) * sizeof(int));
+      align_up((static_cast<size_t>(kHdrPref) + 2 * batch + 1 + n_pairs + 1) * sizeof(int));
   const size_t lse = align_up(slots * kMlaHeads * sizeof(float));
   const size_t o = align_up(slots * kMlaHeads * kMlaDc * sizeof(float));
   if (off_lse) *off_lse = hdr;

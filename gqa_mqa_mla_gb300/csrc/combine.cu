@@ -97,14 +97,15 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) lse_combine_kernel(const Com
 }
 
 // MLA partials of a balanced schedule: sequence b's tiles [g0, g1) were cut
-// by the pair slices [starts[q], starts[q + 1]) (the slice-start table the
-// partial kernel writes after the per-sequence first-tile table).  Only the
-// first and the last segment of a slice can be partial, and pair q writes
-// them to slots 2 q and 2 q + 1: b's piece in its first pair q0 is slot
-// 2 q0 + 1 unless b starts that slice, and its piece in every later pair
-// starts that pair's slice (slot 2 q).  Rows of sequences that one pair
-// covered whole (or that have no tiles) were written by the partial kernel
-// and are skipped.  One warp per (sequence, head).
+// by the pair slices [starts[q], starts[q + 1]) (the partial kernel writes
+// the slice starts and every sequence's first cost position after the
+// per-sequence first-tile table).  Only the first and the last segment of a
+// slice can be partial, and pair q writes them to slots 2 q and 2 q + 1: b's
+// piece in its first pair q0 is slot 2 q0 + 1 unless b starts that slice,
+// and its piece in every later pair starts that pair's slice (slot 2 q).
+// Rows of sequences that one pair covered whole (or that have no tiles)
+// were written by the partial kernel and are skipped.  One warp per
+// (sequence, head).
 template <bool kBF16>
 __global__ void __launch_bounds__(kRowsPerCta * 32) mla_combine_kernel(const MlaCombineParams p) {
   wait_for_partials();
@@ -114,20 +115,11 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) mla_combine_kernel(const Mla
   const int g0 = p.ws_hdr[kHdrPref + b], g1 = p.ws_hdr[kHdrPref + b + 1];
   if (g1 <= g0) return;
   const int* starts = p.ws_hdr + kHdrPref + p.batch + 1;
-  // The pair holding tile g: the last q with starts[q] <= g (starts[0] = 0,
-  // non-decreasing; a pair with an empty slice shares its start with the next).
-  auto pair_of = [&](int g) {
-    int lo = 0, hi = p.n_pairs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (starts[mid] <= g)
-        lo = mid;
-      else
-        hi = mid - 1;
-    }
-    return lo;
-  };
-  const int q0 = pair_of(g0), q1 = pair_of(g1 - 1);
+  const int* cprefs = starts + p.n_pairs + 1;
+  // The pair holding tile g is the one whose cost slice holds g's cost
+  // position: q = min(c(g) / W, n_pairs - 1), c(b's first tile) = cprefs[b].
+  const int W = p.ws_hdr[0], cb = cprefs[b];
+  const int q0 = min(cb / W, p.n_pairs - 1), q1 = min((cb + g1 - g0 - 1) / W, p.n_pairs - 1);
   if (q1 == q0) return;
   const int first_slot = 2 * q0 + (g0 == starts[q0] ? 0 : 1);
   auto row = [=](int s) {

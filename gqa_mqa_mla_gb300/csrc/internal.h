@@ -41,8 +41,9 @@ struct GqaParams {
 
 // MLA workspace (n_pairs > 1): a header of kHdrPref ints (slice width in
 // cost units, total tiles), the first-tile index of every sequence (batch + 1
-// ints), the first tile of every pair's slice (n_pairs + 1 ints), then the
-// partial log2-sum-exps and outputs of 2 n_pairs slots.
+// ints), the first tile of every pair's slice (n_pairs + 1 ints), the cost
+// position of every sequence's first tile (batch ints), then the partial
+// log2-sum-exps and outputs of 2 n_pairs slots.
 constexpr int kHdrPref = 64;
 
 struct MlaParams {

@@ -397,6 +397,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // sequence starts there; a target in the gap before a sequence starts
     // at its first tile; targets past the last tile start at t_all.
     int* starts = p.ws_hdr ? p.ws_hdr + kHdrPref + p.batch + 1 : nullptr;  // [n_pairs + 1]
+    int* cprefs = starts ? starts + sc.n_pairs + 1 : nullptr;               // [batch]
     const bool table = starts && sc.pair == 0 && rank == 0;
     if (threadIdx.x == 0) {
       s_misc[2] = t_all;
@@ -410,6 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int64_t lo_c = sc.pair * W, hi_c = lo_c + W;
       for (int b = b_a; b < b_b; ++b) {
         const int n = seq_tiles(p, p.seq_lens[b]);
+        if (table) cprefs[b] = pref + kSegCost * r;  // cost position of b's first tile
         if (n > 0) {
           const int64_t cpref = pref + static_cast<int64_t>(kSegCost) * r;
           const int64_t prev_end = r == 0 ? -1 : cpref - kSegCost - 1;  // previous sequence's last tile
