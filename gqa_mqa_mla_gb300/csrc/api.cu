@@ -433,7 +433,18 @@ static int gqa_decode_impl(const void* q, const void* k_cache, const void* v_cac
         !make_map_2d_t(&tv, v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, rows_total,
                        row_bytes, kHeadDim, box_rows))
       return DECATTN_ERR_CUDA;
+  } else if (h_q / h_kv <= kWideGroup) {
+    // The CUDA-core / mma.sync consumers: a 3-D view [2 h_kv halves][rows][64]
+    // (strides: a token row, then 128 B per 64-column half), so that one box
+    // brings box_rows rows of both halves of a KV head (landing half-major).
+    const uint64_t row_bytes = static_cast<uint64_t>(h_kv) * kHeadDim * 2;
+    if (!make_map_3d_strided(&tk, k_cache, bf16, 64, rows_total, 2 * static_cast<uint64_t>(h_kv),
+                             row_bytes, 128, 64, box_rows, 2) ||
+        !make_map_3d_strided(&tv, v_cache, bf16, 64, rows_total, 2 * static_cast<uint64_t>(h_kv),
+                             row_bytes, 128, 64, box_rows, 2))
+      return DECATTN_ERR_CUDA;
   } else {
+    // The tcgen05 kernel of wide groups: 2-D boxes of one 64-column half.
     const uint64_t row_bytes = static_cast<uint64_t>(h_kv) * kHeadDim * 2;
     if (!make_map_2d(&tk, k_cache, bf16, static_cast<uint64_t>(h_kv) * kHeadDim, rows_total,
                      row_bytes, 64, box_rows) ||

@@ -55,9 +55,14 @@ constexpr int kKvTileBytes = 2 * kHalfBytes;    // 16 KB
 constexpr int kStageBytes = 2 * kKvTileBytes;   // K + V: 32 KB
 constexpr float kNegInf = -__builtin_huge_valf();
 
-// Byte offset of 16-byte chunk c (0..15) of token row r (0..63) in a K or V tile.
-__device__ __forceinline__ uint32_t tile_off(int r, int c) {
-  return static_cast<uint32_t>((c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// Byte offset of 16-byte chunk c (0..15) of token row r (0..63) in a 16-bit
+// K or V tile.  The tile lands in groups of R = min(block size, 64) rows
+// (lg_r = log2 R), one box per group holding both 64-column halves: group
+// r / R at (r / R) 2R x 128 B, half c / 8 R x 128 B into it, then row
+// r % R; R = 64 is the plain [2 halves][64 rows][128 B] layout.
+__device__ __forceinline__ uint32_t tile_off(int r, int c, int lg_r) {
+  return static_cast<uint32_t>((((r >> lg_r) + (c >> 3)) << (lg_r + 7)) + r * 128 +
+                               (((c & 7) ^ (r & 7)) << 4));
 }
 
 // ------------------------------------------------------------------ CUDA-core consumer
@@ -72,12 +77,13 @@ struct CcConsumer {
   float q[G][8];
   float o[G][8];
   float m[G], l[G];
-  int chunk, half, cw;
+  int chunk, half, cw, lg_r;
 
   __device__ __forceinline__ void init(const GqaParams& p, int b, int j, int cw_, int lane) {
     cw = cw_;
     chunk = lane & 15;  // 16-byte chunk of the 256-byte row: d = chunk*8 .. chunk*8+7
     half = lane >> 4;   // the two half-warps take alternate tokens
+    lg_r = min(p.log2_block_size, 6);
     const uint16_t* qb = static_cast<const uint16_t*>(p.q);
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -113,7 +119,7 @@ struct CcConsumer {
     for (int i = 0; i < 8; ++i) {
       const int r = cw * 16 + 2 * i + half;
       float k[8];
-      load8(ks + tile_off(r, chunk), k);
+      load8(ks + tile_off(r, chunk, lg_r), k);
       float part[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -149,7 +155,7 @@ struct CcConsumer {
       const int r = cw * 16 + 2 * i + half;
       if (static_cast<unsigned>(r - nskip) < span) {
         float v[8];
-        load8(vs + tile_off(r, chunk), v);
+        load8(vs + tile_off(r, chunk, lg_r), v);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float pr = ex2(s[i][g] - m[g]);
@@ -208,11 +214,12 @@ struct MmaConsumer {
   uint32_t qa[8][4];  // A fragments of the padded query group, 8 k-steps of 16
   float o[16][4];     // 16 n-tiles of 8 head dims, rows (lane/4, lane/4+8)
   float m[2], l[2];
-  int mt, tok0, cw, lane;
+  int mt, tok0, cw, lane, lg_r;
 
   __device__ __forceinline__ void init(const GqaParams& p, int b, int j, int cw_, int lane_) {
     cw = cw_;
     lane = lane_;
+    lg_r = min(p.log2_block_size, 6);
     mt = cw % MT;
     tok0 = (cw / MT) * kTokensPerWarp;
     const int G = p.group;
@@ -254,7 +261,7 @@ struct MmaConsumer {
         for (int idx = lane; idx < (lo + hi) * 16; idx += 32) {
           const int k = idx >> 4;
           const int r = k < lo ? r0 + k : nval + (k - lo);
-          *reinterpret_cast<uint4*>(vs + tile_off(r, idx & 15)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vs + tile_off(r, idx & 15, lg_r)) = make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
       }
@@ -266,7 +273,7 @@ struct MmaConsumer {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(ks_base + tile_off(tok, 2 * ks + (mi & 1)), b0, b1, b2, b3);
+          ldsm_x4(ks_base + tile_off(tok, 2 * ks + (mi & 1), lg_r), b0, b1, b2, b3);
           mma_16816<kBF16>(s0, qa[ks], b0, b1);
           mma_16816<kBF16>(s1, qa[ks], b2, b3);
         }
@@ -314,7 +321,7 @@ struct MmaConsumer {
 #pragma unroll
         for (int dp = 0; dp < 8; ++dp) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(vs_base + tile_off(tok, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+          ldsm_x4_trans(vs_base + tile_off(tok, 2 * dp + (mi >> 1), lg_r), b0, b1, b2, b3);
           mma_16816<kBF16>(o[2 * dp], pa, b0, b1);
           mma_16816<kBF16>(o[2 * dp + 1], pa, b2, b3);
         }
@@ -783,23 +790,22 @@ __global__ void __launch_bounds__(32 * (1 + Consumer::kWarps), Consumer::kMinBlo
             }
           }
         } else if (bs >= kTile) {
+          // One box per tile and tensor: 64 rows x both 64-column halves of
+          // KV head j (3-D map [2 h_kv halves][rows][64], half-major landing).
           const int row = bt[t0 >> p.log2_block_size] * bs + (t0 & (bs - 1));
           mbar_arrive_expect_tx(fb, kStageBytes);
-          tma_load_2d_hint(st, &tm_k, x0, row, fb, policy);
-          tma_load_2d_hint(st + kHalfBytes, &tm_k, x0 + 64, row, fb, policy);
-          tma_load_2d_hint(st + kKvTileBytes, &tm_v, x0, row, fb, policy);
-          tma_load_2d_hint(st + kKvTileBytes + kHalfBytes, &tm_v, x0 + 64, row, fb, policy);
+          tma_load_3d_hint(st, &tm_k, 0, row, 2 * j, fb, policy);
+          tma_load_3d_hint(st + kKvTileBytes, &tm_v, 0, row, 2 * j, fb, policy);
         } else {
+          // One box per block and tensor: its bs rows x both halves.
           const int nblk = (nval + bs - 1) >> p.log2_block_size;
-          const int box = bs * 128;
-          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nblk * 4 * box));
+          const int box = 2 * bs * 128;
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nblk * 2 * box));
           for (int k = 0; k < nblk; ++k) {
             const int row = bt[(t0 >> p.log2_block_size) + k] * bs;
             const uint32_t off = static_cast<uint32_t>(k * box);
-            tma_load_2d_hint(st + off, &tm_k, x0, row, fb, policy);
-            tma_load_2d_hint(st + kHalfBytes + off, &tm_k, x0 + 64, row, fb, policy);
-            tma_load_2d_hint(st + kKvTileBytes + off, &tm_v, x0, row, fb, policy);
-            tma_load_2d_hint(st + kKvTileBytes + kHalfBytes + off, &tm_v, x0 + 64, row, fb, policy);
+            tma_load_3d_hint(st + off, &tm_k, 0, row, 2 * j, fb, policy);
+            tma_load_3d_hint(st + kKvTileBytes + off, &tm_v, 0, row, 2 * j, fb, policy);
           }
         }
         ++issued;
@@ -887,8 +893,6 @@ cudaError_t launch_one(const GqaParams& p, const CUtensorMap& tk, const CUtensor
   return cudaGetLastError();
 }
 
-// Groups wider than this run on the tcgen05 kernel (gqa_wide.cu).
-constexpr int kWideGroup = 16;
 
 template <bool kBF16>
 cudaError_t dispatch(const GqaParams& p, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -110,6 +110,11 @@ cudaError_t launch_gqa_partial(const GqaParams& p, const CUtensorMap& tm_k,
                                cudaStream_t stream);
 // The tcgen05 partial kernel for wide groups (up to 64 query heads per KV
 // head) over a 16-bit cache; the same maps and outputs as launch_gqa_partial.
+// Query heads per KV head above which the GQA partials run on the tcgen05
+// kernel (gqa_wide.cu); up to it, on the CUDA-core / mma.sync consumers of
+// gqa_decode.cu, whose 16-bit tensor maps differ (see api.cu).
+constexpr int kWideGroup = 16;
+
 cudaError_t launch_gqa_wide_partial(const GqaParams& p, const CUtensorMap& tm_k,
                                     const CUtensorMap& tm_v, bool bf16, cudaStream_t stream);
 // The same over an e4m3 cache (the 8-bit maps of launch_gqa_partial_fp8).

@@ -198,6 +198,15 @@ DECATTN_DEV void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, i
 }
 
 // 3-D tiled bulk tensor load global -> shared (x innermost).
+DECATTN_DEV void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                  uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 DECATTN_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
                              uint32_t bar) {
   asm volatile(
