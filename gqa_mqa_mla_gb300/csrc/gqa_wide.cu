@@ -17,8 +17,9 @@
 // Operand placement:
 //   Q_j        shared memory, [2 halves][64 rows][128 B], 128-byte swizzled
 //              K-major, written once by the softmax threads    A of S
-//   K, V tiles TMA ring (kStages), the same [2 halves][64 tokens][128 B]
-//              swizzled layout as the other GQA kernels: K     B of S (K-major)
+//   K, V tiles TMA ring (kStages), [2 halves][64 tokens][128 B], 128-byte
+//              swizzled, one box per 64-column half and block:
+//                                                     K        B of S (K-major)
 //                                                     V        B of PV (MN-major)
 //   P(j)       shared memory, [64 rows][64 tokens x 2 B], two buffers  A of PV
 //   S(j)       TMEM, two buffers of 64 fp32 columns
@@ -37,9 +38,10 @@
 //   8    TMA producer of the K tiles (walks the block table); a K stage is
 //        free again once S(j) has read it;
 //   10   TMA producer of the V tiles; a V stage is free after PV(j).
-//   9    TMEM allocator and MMA issuer (one elected lane): S(j + 1) is issued
-//        as soon as its K tile has landed and its S buffer is read, so that
-//        it runs while the softmax works on tile j; O += P(j) V(j) follows.
+//   9    TMEM allocator and MMA issuer (one elected lane): S(j + 1) (its K
+//        tile landed, its S buffer read) and O += P(j) V(j) (P(j) written)
+//        go in whichever order their operands arrive, S first when both are
+//        ready, so that S(j + 1) runs while the softmax works on tile j.
 // While an MMA runs, threads touch only TMEM columns and shared memory it
 // neither reads nor writes: S(j + 1) (S buffer (j + 1) & 1, K) runs while the
 // softmax writes P(j) and zeroes stale V(j) rows; O is rescaled only after
@@ -48,8 +50,9 @@
 //
 // An 8-bit (e4m3) cache takes the same pipeline with three changes: the K
 // stage, as it lands, is the B operand of S = Q K^T on kind::f8f6f4, whose A
-// operand is Q split into e4m3 terms (two for a bf16 query, three for fp16:
-// exact, scaled per row by a power of two that the softmax undoes); the
+// operand is Q split into e4m3 terms (two for a bf16 query, three for fp16,
+// each row scaled by a power of two that the softmax undoes: exact except
+// for parts below 2^-18 of the row's largest element); the
 // softmax threads convert each landed V tile into one of two 16-bit slabs
 // (e4m3 -> f16 is exact) before they publish P(j), the slab being the B
 // operand of O += P V on f16; and the rings hold two 8 KB stages.  A
