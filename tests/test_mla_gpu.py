@@ -204,3 +204,17 @@ def test_single_long_sequence_over_every_pair():
     x = synth.mla_inputs(batch=1, seq_lens=[65536], block_size=64, seed=79, device=DEV)
     _check(x, 0, n_rows=128, what="B=1 S=64k auto")
     _check(x, 7, n_rows=64, what="B=1 S=64k 7 pairs")
+
+
+def test_cost_gaps_leave_pairs_without_tiles():
+    """Many one-tile sequences and more pairs than the tile count can feed: the
+    per-sequence cost gaps of the schedule give some pairs empty slices, and
+    zero-length sequences in between must still be zeroed exactly once."""
+    lens = [1, 64, 0, 33, 64, 1, 0, 0, 50, 64, 2, 64, 0, 10, 64, 64, 5, 0, 64, 1] * 2
+    x = synth.mla_inputs(batch=len(lens), seq_lens=lens, block_size=64, seed=80, device=DEV)
+    for ns in (76, 40, 23, 9):
+        _check(x, ns, n_rows=len(lens) * 128, what=f"cost gaps pairs={ns}")
+    out = _run(x, 76)
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert torch.all(out[b] == 0)
