@@ -54,7 +54,11 @@ __device__ __forceinline__ void merge_row(const float* lse, const float* po, Row
     // Weight of partial s0 + lane: 2^(lse - max), 0 for an empty split.
     const float wl = lane < cnt ? ex2(lse[row(s0 + lane)] - mx) : 0.f;
     wsum += wl;
-#pragma unroll 4
+    // All of a row's partial loads in flight at once where registers allow
+    // (long context merges 32 splits of 128 values: 16 in flight against 4,
+    // 88.9 against 91.7 us for the whole B = 1, S = 131072 call).
+    constexpr int kUnroll = kVec == 1 ? 16 : 4;
+#pragma unroll kUnroll
     for (int i = 0; i < cnt; ++i) {
       const float w = __shfl_sync(kFull, wl, i);
       const size_t base = row(s0 + i) * (D / 4);
