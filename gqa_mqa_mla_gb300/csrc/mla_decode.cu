@@ -38,17 +38,21 @@
 // the score chunks (4-4r..7-4r, then the RoPE chunk 8) and positions 5-8 the
 // value chunks, so that one instruction sequence serves both CTAs.
 // Operand placement (per CTA):
-//   Q, positions 0-4   TMEM, 160 columns (two 16-bit values per column)  A of S
-//   Q, positions 5-8   shared memory (TMA), 128-byte swizzled K-major    A of S
+//   Q, positions 0-2, 4  TMEM, 128 columns (two 16-bit values per column) A of S
+//   Q, positions 3, 5-8  shared memory (TMA), 128-byte swizzled K-major  A of S
 //   cache tiles        shared memory ring, 2 stages x 64 tokens x 9     B of S;
 //                      chunk slots in position order                    positions 5-8: B of PV
-//   P(j)               TMEM, 32 columns                                 A of PV
+//   S(j), P(j)         TMEM, two 64-column buffers (j % 2): S in fp32,  A of PV (P)
+//                      then P(j) (16-bit) over its first 32 columns
 //   epilogue           the ring stage of the segment's last tile
-// TMEM columns: O [0, 256) | Q [256, 416) | S [416, 480) | P [480, 512).
-// While an MMA runs, threads touch only TMEM columns it neither reads nor
-// writes: S(j + 1) (Q, S) runs while the softmax writes P(j) and rescales O;
-// O += P(j) C(j) (P, O) runs while the softmax reads S(j + 1); O is rescaled,
-// and P(j + 1) written, only after O += P(j) C(j) has completed.
+// TMEM columns: O [0, 256) | Q [256, 384) | S/P buffer 0 [384, 448) | buffer 1 [448, 512).
+// With two S buffers the score chain does not wait for the softmax: S(j + 1)
+// runs while the softmax works on S(j); S(j + 2) reuses buffer j % 2 once
+// O += P(j) C(j), the last reader of P(j) there, has completed.  While an MMA
+// runs, threads touch only TMEM columns it neither reads nor writes: the
+// softmax writes P(j) over S(j) only after every softmax thread has loaded
+// S(j); O is rescaled only after O += P(j - 1) C(j - 1) has completed (and
+// before O += P(j) C(j) is issued, which waits for P(j)).
 //
 // Per CTA (352 threads):
 //   warps 0-7  load Q, softmax, epilogue: warp w serves heads
@@ -89,7 +93,8 @@ constexpr int kBoxRows = kT;                    // rows per TMA box: a whole blo
 constexpr int kStages = 2;                      // cache ring depth
 constexpr int kChunk = 64;                      // columns per 128-byte swizzle row
 constexpr int kChunks = kMlaWidth / kChunk;     // 9 column chunks per cache row
-constexpr int kQSmemChunks = 4;                 // Q positions 5-8 (value chunks) in shared memory
+constexpr int kQSmemChunks = 5;                 // Q positions 5-8 (value chunks) and 3 in shared memory
+constexpr int kQPos3Slot = 4;                   // shared-memory Q chunk slot of position 3
 constexpr int kValueSlot = 5;                   // ring slot (position) of the first value chunk
 constexpr int kQChunkBytes = kMlaHeads * 128;   // [128 heads][64 cols] = 16 KB
 constexpr int kCChunkBytes = kT * 128;          // [64 tokens][64 cols] = 8 KB
@@ -106,25 +111,24 @@ constexpr int kWarpProducer = 8, kWarpMmaS = 9, kWarpMmaPv = 10;
 constexpr int kThreads = kSoftmaxThreads + 96;
 constexpr int kTmemCols = 512;
 constexpr int kTmemO = 0;
-constexpr int kTmemQ = 256;                     // Q positions 0-4: 160 TMEM columns
-constexpr int kTmemS = 416;                     // S tile: 64 columns fp32
-constexpr int kTmemP = 480;                     // P tile: 64 bf16 = 32 columns
+constexpr int kTmemQ = 256;                     // Q positions 0, 1, 2, 4: 128 TMEM columns
+constexpr int kTmemS = 384;                     // two S / P buffers of 64 columns
 constexpr int kEpiBoxes = 4;                    // 16 KB output boxes staged per round
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when p could exceed 2^8
 
 // mbarrier slots (8 bytes each) inside the barrier area
 enum : int {
-  kBarQ = 0,                               // Q[:, 256:576) in TMEM (256 arrivals)
+  kBarQ = 0,                               // Q's TMEM positions written (256 arrivals)
   kBarFullS = 1,                           // kStages: score chunks landed (TMA bytes)
   kBarFullV = kBarFullS + kStages,         // kStages: value chunks landed (TMA bytes)
   kBarEmptyS = kBarFullV + kStages,        // kStages: score chunks free again
   kBarEmptyV = kBarEmptyS + kStages,       // kStages: value chunks free again
-  kBarSFull = kBarEmptyV + kStages,        // S(j) computed
-  kBarSFree = kBarSFull + 1,               // S(j) read by the softmax (256 arrivals)
-  kBarPFull = kBarSFree + 1,               // P(j) written (256 arrivals)
-  kBarPvDone = kBarPFull + 1,              // O += P(j) C_lat(j) complete
-  kBarQs = kBarPvDone + 1,                 // Q[:, 0:256) in shared memory (TMA)
+  kBarSFull = kBarEmptyV + kStages,        // 2 (buffer j % 2): S(j) computed
+  kBarSRead = kBarSFull + 2,               // 2: S(j) loaded by every softmax thread (256 arrivals)
+  kBarPFull = kBarSRead + 2,               // 2: P(j) written (256 arrivals)
+  kBarPvDone = kBarPFull + 2,              // 2: O += P(j) C_lat(j) complete
+  kBarQs = kBarPvDone + 2,                 // Q's shared-memory chunks landed (TMA)
   kBarQFree = kBarQs + 1,                  // a segment's last S done: Q may be replaced
   kBarSum = kBarQFree + 1,                 // row sums exchanged (256 arrivals)
   kBarEpiW = kBarSum + 1,                  // epilogue round staged in smem (256 arrivals)
@@ -136,7 +140,10 @@ enum : int {
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kEpiBoxes * kQChunkBytes <= kStageBytes, "epilogue staging must fit one stage");
-static_assert(kTmemP + kT / 2 <= kTmemCols, "tensor memory columns");
+static_assert(kTmemS + 2 * kT <= kTmemCols, "tensor memory columns");
+
+// TMEM slot (32 columns each) of Q position p = 0, 1, 2 or 4.
+__host__ __device__ constexpr int q_tmem_slot(int pos) { return pos < 3 ? pos : 3; }
 
 // Work schedule.  The batch's 64-token tiles, sequence after sequence, form
 // one list of T_all tiles (an invalid seq_len counts as 0 tiles).  A CTA
@@ -282,11 +289,11 @@ __device__ __noinline__ void prefetch_tile(const Producer& pr, const int32_t* bt
   tma_prefetch_l2_2d(pr.tm_c, 8 * kChunk, row);
 }
 
-// The score chain S = Q C(stage)^T over the 9 chunk positions: positions 0-4
-// (score chunks) take Q from TMEM, positions 5-8 (value chunks) from shared
-// memory.  `part` 0 issues positions 0-4 (the first MMA overwrites S), part 1
-// positions 5-8.  Fully unrolled: the issue rate of this single thread bounds
-// the chain.
+// The score chain S = Q C(stage)^T over the 9 chunk positions: positions
+// 0-2 and 4 take Q from TMEM, positions 3 and 5-8 from shared memory.
+// `part` 0 issues positions 0-4 (the score chunks; the first MMA overwrites
+// S), part 1 positions 5-8 (the value chunks).  Fully unrolled: the issue
+// rate of this single thread bounds the chain.
 template <bool kBF16>
 __device__ __forceinline__ void issue_score_part(int part, uint32_t d, uint32_t tmem, uint64_t dq,
                                                  uint64_t db) {
@@ -297,9 +304,14 @@ __device__ __forceinline__ void issue_score_part(int part, uint32_t d, uint32_t 
 #pragma unroll
     for (int pos = 0; pos < kValueSlot; ++pos)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc_mma_f16_ts(d, tmem + kTmemQ + pos * 32 + ks * 8, db + pos * kCChunkUnits + 2 * ks, idesc,
-                      (pos > 0 || ks > 0) ? 1u : 0u);
+      for (int ks = 0; ks < 4; ++ks) {
+        if (pos == 3)
+          tc_mma_f16(d, dq + kQPos3Slot * kQChunkUnits + 2 * ks, db + pos * kCChunkUnits + 2 * ks,
+                     idesc, 1u);
+        else
+          tc_mma_f16_ts(d, tmem + kTmemQ + q_tmem_slot(pos) * 32 + ks * 8,
+                        db + pos * kCChunkUnits + 2 * ks, idesc, (pos > 0 || ks > 0) ? 1u : 0u);
+      }
   } else {
 #pragma unroll
     for (int pos = kValueSlot; pos < kChunks; ++pos)
@@ -469,10 +481,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarEmptyS + s), 1);
       mbar_init(bar(kBarEmptyV + s), 1);
     }
-    mbar_init(bar(kBarSFull), 1);
-    mbar_init(bar(kBarSFree), kSoftmaxThreads);
-    mbar_init(bar(kBarPFull), kSoftmaxThreads);
-    mbar_init(bar(kBarPvDone), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarSFull + i), 1);
+      mbar_init(bar(kBarSRead + i), kSoftmaxThreads);
+      mbar_init(bar(kBarPFull + i), kSoftmaxThreads);
+      mbar_init(bar(kBarPvDone + i), 1);
+    }
     mbar_init(bar(kBarEpiW), kSoftmaxThreads);
     mbar_init(bar(kBarEpiR), 1);
     mbar_init(bar(kBarDrainS), 1);
@@ -528,16 +542,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (sg.kind == kSegZero) continue;
         const int n = (sg.t1 - sg.t0 + kT - 1) / kT;
         const int32_t* bt = p.block_table + static_cast<size_t>(sg.b) * p.max_blocks_per_seq;
-        // Q[:, 0:256) of this segment's sequence, once the previous
-        // segment's last S (the last reader of the Q region) has completed;
-        // this overlaps the previous segment's epilogue.
+        // Q's shared-memory chunks (this CTA's value columns and position 3)
+        // of this segment's sequence, once the previous segment's last S (the
+        // last reader of the Q region) has completed; this overlaps the
+        // previous segment's epilogue.
         if (q_issued > 0 &&
             !mbar_wait_or_abort(bar(kBarQFree), (q_issued - 1) & 1, p.err_flag, abort_word)) {
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(bar(kBarQs), kQSmemChunks * kQChunkBytes);
-        for (int c = 0; c < kQSmemChunks; ++c)
+        tma_load_2d(sbase + kOffQ + kQPos3Slot * kQChunkBytes, &tm_qa,
+                    chunk_at(static_cast<int>(rank), 3) * kChunk, sg.b * kMlaHeads, bar(kBarQs));
+        for (int c = 0; c < 4; ++c)
           tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_qa, (4 * static_cast<int>(rank) + c) * kChunk, sg.b * kMlaHeads,
                       bar(kBarQs));
         ++q_issued;
@@ -592,19 +609,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int gi = g + j;
         const int s = gi % kStages;
         const uint32_t ph = static_cast<uint32_t>(gi / kStages) & 1u;
-        // S is one TMEM tile: S(gi) waits until the softmax has read S(gi - 1).
-        ok = (gi == 0 || wait(kBarSFree, (gi - 1) & 1)) && wait(kBarFullS + s, ph);
+        // S(gi) goes to buffer gi % 2 once O += P(gi - 2) C(gi - 2) (the last
+        // reader of P(gi - 2) there) has completed.
+        const uint32_t sbuf = tmem + kTmemS + 64 * (gi & 1);
+        ok = (gi < 2 || wait(kBarPvDone + (gi & 1), ((gi - 2) >> 1) & 1)) && wait(kBarFullS + s, ph);
         if (!ok) break;
         tc_fence_after();
         const uint64_t db = dr + static_cast<uint64_t>(s) * kStageUnits;
-        if (elect_one()) issue_score_part<kBF16>(0, tmem + kTmemS, tmem, dq, db);
+        if (elect_one()) issue_score_part<kBF16>(0, sbuf, tmem, dq, db);
         __syncwarp();
         ok = wait(kBarFullV + s, ph);
         if (!ok) break;
         tc_fence_after();
         if (elect_one()) {
-          issue_score_part<kBF16>(1, tmem + kTmemS, tmem, dq, db);
-          tc_commit(bar(kBarSFull));
+          issue_score_part<kBF16>(1, sbuf, tmem, dq, db);
+          tc_commit(bar(kBarSFull + (gi & 1)));
           // Q may be replaced once a segment's last S has completed.
           tc_commit(bar(j + 1 < n ? kBarEmptyS + s : kBarQFree));
         }
@@ -635,7 +654,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < n; ++j) {
         const int gi = g + j;
         bool w = true;
-        if (lane == 0) w = mbar_wait_or_abort(bar(kBarPFull), gi & 1, p.err_flag, abort_word);
+        if (lane == 0)
+          w = mbar_wait_or_abort(bar(kBarPFull + (gi & 1)), (gi >> 1) & 1, p.err_flag, abort_word);
         ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
         if (!ok) break;
         tc_fence_after();
@@ -645,9 +665,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (elect_one()) {
 #pragma unroll
           for (int ks = 0; ks < kT / 16; ++ks)
-            tc_mma_f16_ts(tmem + kTmemO, tmem + kTmemP + ks * 8, db + ks * (2048 >> 4), idesc_pv,
+            tc_mma_f16_ts(tmem + kTmemO, tmem + kTmemS + 64 * (gi & 1) + ks * 8,
+                          db + ks * (2048 >> 4), idesc_pv,
                           (j > 0 || ks > 0) ? 1u : 0u);
-          tc_commit(bar(kBarPvDone));
+          tc_commit(bar(kBarPvDone + (gi & 1)));
           if (j + 1 < n) tc_commit(bar(kBarEmptyV + gi % kStages));
         }
         __syncwarp();
@@ -666,37 +687,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float* red_sum = reinterpret_cast<float*>(smem + kOffRed);       // [2 halves][128]
     const float scale = p.scale_log2;
-    // Q row h of sequence b at positions 0-4 (this CTA's score chunks) into
-    // TMEM (positions 5-8 arrive in shared memory by TMA); the two halves
-    // split the five 64-column chunks 3 + 2, all loads in flight before any
-    // store.  Called only while no MMA reads the Q columns (before the
-    // segment's first S, after the previous segment's last S has completed).
+    // Q row h of sequence b at positions 0, 1, 2 and 4 into TMEM (positions
+    // 3 and 5-8 arrive in shared memory by TMA); the two halves take two
+    // positions each, all loads in flight before any store.  Called only
+    // while no MMA reads the Q columns (before the segment's first S, after
+    // the previous segment's last S has completed).
     auto load_q_tmem = [&](int b) {
       const size_t row = static_cast<size_t>(b) * kMlaHeads + h;
       const uint4* qa = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_abs) +
                                                        row * kMlaDc);
       const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q_rope) +
                                                        row * kMlaDr);
-      const int p0 = ch == 0 ? 0 : 3, np = ch == 0 ? 3 : 2;
-      uint4 w[24];
+      const int pos2[2] = {ch == 0 ? 0 : 2, ch == 0 ? 1 : 4};
+      uint4 w[16];
 #pragma unroll
-      for (int kk = 0; kk < 24; ++kk) {
-        const int c = chunk_at(static_cast<int>(rank), p0 + kk / 8);
-        if (kk < np * 8) w[kk] = c < 8 ? qa[c * 8 + kk % 8] : qr[kk % 8];
+      for (int kk = 0; kk < 16; ++kk) {
+        const int c = chunk_at(static_cast<int>(rank), pos2[kk / 8]);
+        w[kk] = c < 8 ? qa[c * 8 + kk % 8] : qr[kk % 8];
       }
 #pragma unroll
-      for (int cc = 0; cc < 3; ++cc) {
-        if (cc < np) {
-          float v[32];
+      for (int cc = 0; cc < 2; ++cc) {
+        float v[32];
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            v[4 * kk] = __uint_as_float(w[cc * 8 + kk].x);
-            v[4 * kk + 1] = __uint_as_float(w[cc * 8 + kk].y);
-            v[4 * kk + 2] = __uint_as_float(w[cc * 8 + kk].z);
-            v[4 * kk + 3] = __uint_as_float(w[cc * 8 + kk].w);
-          }
-          tmem_st32(tmem + lane_base + kTmemQ + (p0 + cc) * 32, v);
+        for (int kk = 0; kk < 8; ++kk) {
+          v[4 * kk] = __uint_as_float(w[cc * 8 + kk].x);
+          v[4 * kk + 1] = __uint_as_float(w[cc * 8 + kk].y);
+          v[4 * kk + 2] = __uint_as_float(w[cc * 8 + kk].z);
+          v[4 * kk + 3] = __uint_as_float(w[cc * 8 + kk].w);
         }
+        tmem_st32(tmem + lane_base + kTmemQ + q_tmem_slot(pos2[cc]) * 32, v);
       }
       tc_wait_st();
       tc_fence_before();
@@ -741,7 +760,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int gj = g + j;
         const int nval = min(kT, sg.t1 - (sg.t0 + j * kT));
         const int nv = nval - ch * 32;  // valid columns in this half (may be <= 0 or > 32)
-        if (!mbar_wait_or_abort(bar(kBarSFull), gj & 1, p.err_flag, abort_word)) {
+        const int sb = gj & 1;                        // S / P buffer of this tile
+        const uint32_t sp_phase = static_cast<uint32_t>(gj >> 1) & 1u;
+        if (!mbar_wait_or_abort(bar(kBarSFull + sb), sp_phase, p.err_flag, abort_word)) {
           ok = false;
           break;
         }
@@ -749,11 +770,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // This thread's 32 score columns, and the partner half's, from which
         // both threads of the row take the same full-row maximum (no exchange).
         float s[32], so[32];
-        tmem_ld32(tmem + lane_base + kTmemS + ch * 32, s);
-        tmem_ld32(tmem + lane_base + kTmemS + (ch ^ 1) * 32, so);
+        tmem_ld32(tmem + lane_base + kTmemS + 64 * sb + ch * 32, s);
+        tmem_ld32(tmem + lane_base + kTmemS + 64 * sb + (ch ^ 1) * 32, so);
         tc_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar(kBarSFree));  // the score issuer may now compute S(j + 1)
+        mbar_arrive(bar(kBarSRead + sb));  // P(j) may overwrite S(j) once all have loaded it
         // Tile max of the scaled scores over the row (masked columns ignored).
         const int nvo = nval - (ch ^ 1) * 32;  // valid columns of the partner half
         const float lowest = scale >= 0.f ? kNegInf : -kNegInf;
@@ -777,19 +798,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             so[kk] = scale >= 0.f ? fmaxf(so[kk], so[kk + w]) : fminf(so[kk], so[kk + w]);
         float mt = so[0] * scale;
         if (mt != mt) mt = kNegInf;  // an all-masked row (-inf * 0 cannot occur: scale != 0)
-        // O += P(j - 1) C(j - 1) must have completed before P(j) is written
-        // or O is rescaled.  (The previous segment's last one was waited for
-        // by its epilogue.)
-        if (j > 0 &&
-            !mbar_wait_or_abort(bar(kBarPvDone), (gj - 1) & 1, p.err_flag, abort_word)) {
-          ok = false;
-          break;
-        }
         const bool need = mt > m_used + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? mt : m_used;
           const float factor = need ? ex2(m_used - m_new) : 1.f;  // 0 when m_used = -inf
           if (j > 0) {
+            // O += P(j - 1) C(j - 1) must have completed before O is rescaled.
+            // (The previous segment's last one was waited for by its epilogue.)
+            if (!mbar_wait_or_abort(bar(kBarPvDone + ((gj - 1) & 1)), ((gj - 1) >> 1) & 1,
+                                    p.err_flag, abort_word)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
 #pragma unroll 1
             for (int c = ch * 128; c < ch * 128 + 128; c += 32) {
@@ -830,7 +850,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           lt_tile = (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
         l += lt_tile;
-        tmem_st16(tmem + lane_base + kTmemP + ch * 16, pk);
+        // P(j) over the first 32 columns of S(j)'s buffer, once every softmax
+        // thread has loaded S(j) (both threads of a row read all 64 columns).
+        if (!mbar_wait_or_abort(bar(kBarSRead + sb), sp_phase, p.err_flag, abort_word)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st16(tmem + lane_base + kTmemS + 64 * sb + ch * 16, pk);
         if (nval < kT) {
           // Value rows past the sequence end may hold anything (even NaN): zero
           // them so that P = 0 there contributes exactly nothing.  S(j) has
@@ -846,7 +873,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(kBarPFull));
+        mbar_arrive(bar(kBarPFull + sb));
         if (j + 2 == n_tiles) {
           // Pull the next segment's Q rows into L2 for its TMEM load.
           Cursor c2 = cur;
@@ -856,8 +883,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (have) {
             const char* row = reinterpret_cast<const char*>(
                 static_cast<const uint16_t*>(p.q_abs) + (static_cast<size_t>(nx.b) * kMlaHeads + h) * kMlaDc);
-            for (int pos = ch == 0 ? 0 : 3; pos < (ch == 0 ? 3 : 5); ++pos) {
-              const int c = chunk_at(static_cast<int>(rank), pos);
+            for (int i = 0; i < 2; ++i) {
+              const int c = chunk_at(static_cast<int>(rank), i == 0 ? (ch == 0 ? 0 : 2) : (ch == 0 ? 1 : 4));
               if (c < 8)
                 prefetch_l2(row + c * 128);
               else
@@ -885,7 +912,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       red_sum[ch * kMlaHeads + h] = l;
       mbar_arrive(bar(kBarSum));
       ok = mbar_wait_or_abort(bar(kBarSum), k & 1, p.err_flag, abort_word) &&
-           mbar_wait_or_abort(bar(kBarPvDone), g_last & 1, p.err_flag, abort_word);
+           mbar_wait_or_abort(bar(kBarPvDone + (g_last & 1)), (g_last >> 1) & 1, p.err_flag,
+                              abort_word);
       if (!ok) break;
       const float lt = l + red_sum[(ch ^ 1) * kMlaHeads + h];
       tc_fence_after();
