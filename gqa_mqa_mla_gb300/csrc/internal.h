@@ -108,13 +108,17 @@ struct CombineParams {
 cudaError_t launch_gqa_partial(const GqaParams& p, const CUtensorMap& tm_k,
                                const CUtensorMap& tm_v, bool bf16, int num_sms,
                                cudaStream_t stream);
-// The tcgen05 partial kernel for wide groups (up to 64 query heads per KV
-// head) over a 16-bit cache; the same maps and outputs as launch_gqa_partial.
+// The same over an e4m3 KV cache (tm_k / tm_v: 8-bit maps, boxes of 128 B x
+// min(block_size, 64) rows); q / out in fp16 or bf16.
+cudaError_t launch_gqa_partial_fp8(const GqaParams& p, const CUtensorMap& tm_k,
+                                   const CUtensorMap& tm_v, bool bf16, cudaStream_t stream);
 // Query heads per KV head above which the GQA partials run on the tcgen05
 // kernel (gqa_wide.cu); up to it, on the CUDA-core / mma.sync consumers of
 // gqa_decode.cu, whose 16-bit tensor maps differ (see api.cu).
 constexpr int kWideGroup = 16;
 
+// The tcgen05 partial kernel for wide groups (up to 64 query heads per KV
+// head) over a 16-bit cache; the same maps and outputs as launch_gqa_partial.
 cudaError_t launch_gqa_wide_partial(const GqaParams& p, const CUtensorMap& tm_k,
                                     const CUtensorMap& tm_v, bool bf16, cudaStream_t stream);
 // The same over an e4m3 cache (the 8-bit maps of launch_gqa_partial_fp8).
@@ -122,10 +126,6 @@ cudaError_t launch_gqa_wide_partial_fp8(const GqaParams& p, const CUtensorMap& t
                                         const CUtensorMap& tm_v, bool bf16, cudaStream_t stream);
 // tm_out: 16-bit [B * 128, 512] output, boxes of 64 x 128; tm_po: fp32
 // [2 n_pairs * 128, 512] partials, boxes of 32 x 128 (both 128-byte swizzle).
-// The same over an e4m3 KV cache (tm_k / tm_v: 8-bit maps, boxes of 128 B x
-// min(block_size, 64) rows); q / out in fp16 or bf16.
-cudaError_t launch_gqa_partial_fp8(const GqaParams& p, const CUtensorMap& tm_k,
-                                   const CUtensorMap& tm_v, bool bf16, cudaStream_t stream);
 // tm_c4: the latent cache viewed as [9 chunks][rows][64] (chunk stride 128 B,
 // row stride 1152 B), boxes of 64 x 64 rows x 4 chunks: one copy brings four
 // 64-column chunks of a 64-token tile, chunk-major; used when block_size is 64.
