@@ -22,13 +22,16 @@
 // Two consumer flavours:
 //   CcConsumer<G>    CUDA cores, used for MHA (G = 1): a half-warp holds one
 //                    token row (16 lanes x 16 B), warp-shuffle dot products;
-//   MmaConsumer<MT>  tensor cores (mma.sync m16n8k16) for G >= 2: the query
-//                    group padded to 16*MT rows is the A operand, K^T / V the
-//                    B operand read with ldmatrix from the swizzled tile.
+//   MmaConsumer<MT>  tensor cores (mma.sync m16n8k16) for 2 <= G <= 16 (wider
+//                    groups run on the tcgen05 kernel of gqa_wide.cu): the
+//                    query group padded to 16*MT rows is the A operand, K^T / V
+//                    the B operand read with ldmatrix from the swizzled tile.
 //
 // Shared-memory tile layout (written by TMA with 128-byte swizzle): a stage
-// holds K then V; each is two 64-column halves of [64 tokens][128 B], and the
-// 16-byte chunk c of row r sits at chunk (c ^ (r % 8)) of that row.
+// holds K then V; each holds 64 token rows of 256 B in groups of
+// R = min(block size, 64) rows, one box per cache block, a group being
+// [2 column halves][R rows][128 B] (tile_off below); the 16-byte chunk c of a
+// 128-byte row r sits at chunk (c ^ (r % 8)) of that row.
 //
 // 8-bit (e4m3) caches ("Why GQA's KV Cache Savings Don't Fully Reduce TPOT",
 // "When the Serving Engineer Doesn't Get to Choose the Model Architecture":
