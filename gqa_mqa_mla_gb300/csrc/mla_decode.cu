@@ -100,7 +100,7 @@ constexpr int kQChunkBytes = kMlaHeads * 128;   // [128 heads][64 cols] = 16 KB
 constexpr int kCChunkBytes = kT * 128;          // [64 tokens][64 cols] = 8 KB
 constexpr int kStageBytes = kChunks * kCChunkBytes;  // 72 KB
 constexpr int kOffQ = 0;
-constexpr int kOffRing = kOffQ + kQSmemChunks * kQChunkBytes;  // 64 KB
+constexpr int kOffRing = kOffQ + kQSmemChunks * kQChunkBytes;  // 80 KB
 constexpr int kOffBars = kOffRing + kStages * kStageBytes;     // +144 KB
 constexpr int kBarBytes = 256;
 constexpr int kOffRed = kOffBars + kBarBytes;                  // row-sum exchange
