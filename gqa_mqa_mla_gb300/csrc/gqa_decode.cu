@@ -886,22 +886,23 @@ __global__ void __launch_bounds__(32 * (1 + Consumer::kWarps), Consumer::kMinBlo
 
 template <class Consumer, bool kBF16, int kStages>
 cudaError_t launch_one(const GqaParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                       cudaStream_t stream, bool cluster_heads) {
+                       cudaStream_t stream, unsigned max_cluster) {
   auto kern = gqa_partial_kernel<Consumer, kBF16, kStages>;
   constexpr int smem = smem_bytes<Consumer, kStages>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_split, p.h_kv, p.batch);
-  // 16-bit cache: the CTAs of one (split, sequence) read the same cache
-  // blocks, each its KV head's 256-byte rows of every token; launched as
-  // clusters of up to four KV heads they run at the same time on one GPC, so
-  // those reads meet in DRAM.  No cluster feature is used.  Measured on
-  // GB300 (A/B in one process): long context B = 4 with 8 splits 313.5
-  // against 317.8 us, B = 1 with 32 splits 86.9 against 88.2, the 70B layer
-  // and the Llama-3.1-8B layers unchanged; the e4m3 kernel, four CTAs per
-  // SM, lost 1.3 % and launches without clusters.
-  const unsigned cluster =
-      !cluster_heads ? 1u : (p.h_kv % 4 == 0 ? 4u : (p.h_kv % 2 == 0 ? 2u : 1u));
+  // The CTAs of one (split, sequence) read the same cache blocks, each its
+  // KV head's rows of every token (256 B, or 128 B of e4m3 codes); launched
+  // as clusters of up to max_cluster KV heads they run at the same time on
+  // one GPC, so those reads meet in DRAM.  No cluster feature is used.
+  // Measured on GB300 (A/B in one process): 16-bit, clusters of 4: long
+  // context B = 4 with 8 splits 313.5 against 317.8 us, B = 1 with 32
+  // splits 86.9 against 88.2, the 70B layer and the Llama-3.1-8B layers
+  // unchanged; e4m3 70B layer, clusters of 2: 162.6 against 171.9 us and
+  // 164.6 against 168.4 on two GPUs (B = 16: 48.1-48.3 against 51.1-51.4).
+  unsigned cluster = max_cluster;
+  while (cluster > 1 && p.h_kv % cluster != 0) cluster >>= 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(32 * (1 + Consumer::kWarps));
@@ -929,9 +930,9 @@ cudaError_t dispatch(const GqaParams& p, const CUtensorMap& tk, const CUtensorMa
   // the Llama-3.1-8B-shaped GQA layer, 4 heads per KV head: 3.6 TB/s on
   // tensor cores against 2.2 TB/s for the warp-shuffle CUDA-core consumer,
   // which is issue- and latency-bound there).
-  if (p.group == 1) return launch_one<CcConsumer<1, kBF16>, kBF16, S>(p, tk, tv, stream, true);
+  if (p.group == 1) return launch_one<CcConsumer<1, kBF16>, kBF16, S>(p, tk, tv, stream, 4);
   if (p.group <= kWideGroup)
-    return launch_one<MmaConsumer<1, kBF16>, kBF16, S>(p, tk, tv, stream, true);
+    return launch_one<MmaConsumer<1, kBF16>, kBF16, S>(p, tk, tv, stream, 4);
   return launch_gqa_wide_partial(p, tk, tv, kBF16, stream);
 }
 
@@ -939,12 +940,12 @@ template <bool kBF16>
 cudaError_t dispatch_fp8(const GqaParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                          cudaStream_t stream) {
   constexpr int S = 4;  // 16 KB stages: keep as many cache bytes in flight as the 16-bit ring
-  if (p.group == 1) return launch_one<CcConsumerF8<1, kBF16>, kBF16, S>(p, tk, tv, stream, false);
+  if (p.group == 1) return launch_one<CcConsumerF8<1, kBF16>, kBF16, S>(p, tk, tv, stream, 2);
   // Four CTAs per SM of the transposed consumer: three 16 KB stages each.
   if (p.group <= 8)
-    return launch_one<MmaConsumerF8T<1, kBF16>, kBF16, 3>(p, tk, tv, stream, false);
+    return launch_one<MmaConsumerF8T<1, kBF16>, kBF16, 3>(p, tk, tv, stream, 2);
   if (p.group <= kWideGroup)
-    return launch_one<MmaConsumerF8T<2, kBF16>, kBF16, S>(p, tk, tv, stream, false);
+    return launch_one<MmaConsumerF8T<2, kBF16>, kBF16, S>(p, tk, tv, stream, 2);
   return launch_gqa_wide_partial_fp8(p, tk, tv, kBF16, stream);
 }
 
