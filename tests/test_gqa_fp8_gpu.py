@@ -43,6 +43,15 @@ def test_group_sizes_and_splits(h_q, h_kv, num_splits):
     _check(x, num_splits, what=f"h_q={h_q} h_kv={h_kv} splits={num_splits}")
 
 
+@pytest.mark.parametrize("h_q,h_kv", [(5, 5), (6, 3), (20, 5), (12, 6), (28, 7)])
+def test_odd_kv_head_counts(h_q, h_kv):
+    """Odd KV-head counts launch without clusters; even ones in clusters of two."""
+    x = synth.gqa_fp8_inputs(batch=3, h_q=h_q, h_kv=h_kv, seq_lens=[300, 1, 129], block_size=16,
+                             seed=h_q * 13 + h_kv, device=DEV)
+    for ns in (1, 3):
+        _check(x, ns, what=f"h_q={h_q} h_kv={h_kv} splits={ns}")
+
+
 @pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128, 256])
 def test_block_sizes_and_ragged_lengths(block_size):
     lens = [0, 1, 31, 63, 64, 65, 100, 257, 1000]

@@ -62,6 +62,17 @@ def test_group_sizes(h_q, h_kv):
     _check(x, num_splits=3, what=f"h_q={h_q} h_kv={h_kv} splits=3")
 
 
+@pytest.mark.parametrize("h_q,h_kv", [(5, 5), (6, 6), (6, 3), (12, 6), (20, 5), (28, 7),
+                                      (36, 12), (40, 10)])
+def test_kv_head_counts_not_multiples_of_four(h_q, h_kv):
+    """KV-head counts that the launch cannot group four to a cluster: the CTAs
+    of a (split, sequence) run in clusters of two (even counts) or alone."""
+    x = synth.gqa_inputs(batch=3, h_q=h_q, h_kv=h_kv, seq_lens=[300, 1, 129], block_size=16,
+                         dtype="bf16", seed=h_q * 11 + h_kv, device=DEV)
+    _check(x, what=f"h_q={h_q} h_kv={h_kv}")
+    _check(x, num_splits=3, what=f"h_q={h_q} h_kv={h_kv} splits=3")
+
+
 @pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128, 256])
 @pytest.mark.parametrize("h_kv", [2, 1])
 def test_block_sizes_and_ragged_lengths(block_size, h_kv):
