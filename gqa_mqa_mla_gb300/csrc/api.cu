@@ -164,12 +164,12 @@ int plan_splits(int units, int max_seq_len, int slots) {
 // 314 us / 10 splits 456 / 19 splits 325; Llama-3.1-8B MQA (16 units,
 // S <= 4096), 8 splits 32 us / 32 splits 59; its GQA-8 (128 units), 2-3
 // splits 44-45 us / 5 splits 50.
-int plan_splits_one_wave(int units, int max_seq_len, int slots) {
+int plan_splits_one_wave(int units, int max_seq_len, int slots, int min_tiles = 8) {
   const int tiles = max_seq_len > 0 ? (max_seq_len + kTile - 1) / kTile : 1;
   if (units < 1) units = 1;
   if (slots < 1) slots = 1;
   int ns = static_cast<int>((static_cast<int64_t>(slots) * 85) / (100 * static_cast<int64_t>(units)));
-  int cap = tiles / 8 > 1 ? tiles / 8 : 1;
+  int cap = tiles / min_tiles > 1 ? tiles / min_tiles : 1;
   if (cap > DECATTN_MAX_SPLITS) cap = DECATTN_MAX_SPLITS;
   if (ns > cap) ns = cap;
   if (ns < 1) ns = 1;
@@ -182,9 +182,12 @@ int plan_splits_one_wave(int units, int max_seq_len, int slots) {
 int plan_gqa_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms) {
   // GQA partial kernels: two resident CTAs per SM, both the mma.sync one
   // (3-stage ring of 32 KB, up to 16 query heads per KV head) and the
-  // tcgen05 one for wider groups (2-stage K and V rings, ~100 KB).
-  (void)h_q;
-  return plan_splits_one_wave(batch * h_kv, max_seq_len, num_sms * 2);
+  // tcgen05 one for wider groups (2-stage K and V rings, ~100 KB).  The
+  // tcgen05 kernel's splits may be as short as 4 tiles: with few units
+  // (Llama-3.1-8B MQA at B = 16, 16 units, S <= 4096) 16 splits ran 20.7 us
+  // against 22.9 for the 8 that 8-tile splits allow (L2 flushed).
+  const int group = h_kv > 0 ? h_q / h_kv : 1;
+  return plan_splits_one_wave(batch * h_kv, max_seq_len, num_sms * 2, group > kWideGroup ? 4 : 8);
 }
 
 int plan_gqa_fp8_splits(int batch, int h_q, int h_kv, int max_seq_len, int num_sms) {
